@@ -1,0 +1,329 @@
+/*
+ * CPU oracle for the DDTree verify step.  TEST INFRASTRUCTURE ONLY: nothing on
+ * the product path links or calls this file; only the tests, the smoke check
+ * and the benchmark's CPU-baseline leg do.  It shares no code, header, table or
+ * helper with the CUDA library.
+ *
+ * Three plain, slow functions, each written from its definition:
+ *
+ *  ddto_tree_build  best-first draft-tree expansion with a binary heap, as the
+ *                   per-request CPU builder the GPU builder replaces ("The
+ *                   Architecture of a Thousand-Parameter Decision", section
+ *                   "What to Build New", item 3; "The Meta-Cognitive Pivot",
+ *                   the paragraph on moving tree construction off the CPU heapq).
+ *  ddto_attn_rows   tree-verify MLA-absorb attention in float64 for a list of
+ *                   (sequence, node, head) rows ("The Architecture of a
+ *                   Thousand-Parameter Decision", "What to Build New", item 2;
+ *                   "The Milestone Message", section "Architectural Abstraction":
+ *                   the [ones | visibility] mask over positions L + depth).
+ *  ddto_tree_accept greedy follow-the-verified-tree walk ("The Architecture of
+ *                   Closure", the kernel table row for tree_accept.cu).
+ *
+ * Readings taken where the pages are silent (each is a choice, documented in
+ * the design notes): a node is a rank path (r_1..r_d); its score is the float32
+ * sum of the drafter log-probs along the path, added root to leaf with
+ * round-to-nearest and no fused multiply-add; candidates are ordered by score
+ * descending, then depth ascending, then rank path lexicographically
+ * ascending; a -inf candidate is never selected; the root is node 0; node m's
+ * key is KV row T_b + m; a node sees itself; padded rows give zeros and -inf;
+ * among children with equal tokens the lowest index wins; accept_len counts
+ * the root.
+ *
+ * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -shared -fPIC -lm
+ * (no -ffast-math: the tree scores must be IEEE float32 sums).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_BADINPUT 4
+#define MAXD 16
+
+/* ------------------------------------------------------------------ */
+/* tree build                                                          */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    float score;
+    int depth;               /* 1..D */
+    int ranks[MAXD];         /* ranks[0..depth-1] */
+    int parent_node;         /* index of the parent in the output tree */
+} cand_t;
+
+/* negative when a is selected before b */
+static int cand_cmp(const cand_t *a, const cand_t *b) {
+    if (a->score > b->score) return -1;
+    if (a->score < b->score) return 1;
+    if (a->depth != b->depth) return a->depth < b->depth ? -1 : 1;
+    for (int i = 0; i < a->depth; ++i)
+        if (a->ranks[i] != b->ranks[i]) return a->ranks[i] < b->ranks[i] ? -1 : 1;
+    return 0;
+}
+
+static void heap_push(cand_t *h, int *n, const cand_t *c) {
+    int i = (*n)++;
+    h[i] = *c;
+    while (i > 0) {
+        int p = (i - 1) / 2;
+        if (cand_cmp(&h[i], &h[p]) >= 0) break;
+        cand_t t = h[i]; h[i] = h[p]; h[p] = t;
+        i = p;
+    }
+}
+
+static cand_t heap_pop(cand_t *h, int *n) {
+    cand_t top = h[0];
+    h[0] = h[--(*n)];
+    int i = 0;
+    for (;;) {
+        int l = 2 * i + 1, r = l + 1, m = i;
+        if (l < *n && cand_cmp(&h[l], &h[m]) < 0) m = l;
+        if (r < *n && cand_cmp(&h[r], &h[m]) < 0) m = r;
+        if (m == i) break;
+        cand_t t = h[i]; h[i] = h[m]; h[m] = t;
+        i = m;
+    }
+    return top;
+}
+
+/* A drafter row is usable when every log-prob is finite or -inf, <= 0, and
+ * the row is non-increasing; every token must lie in [0, vocab). */
+static int rows_valid(int D, int K, int vocab, const int32_t *tok, const float *lp,
+                      int32_t root) {
+    if (root < 0 || root >= vocab) return 0;
+    for (int d = 0; d < D; ++d) {
+        for (int k = 0; k < K; ++k) {
+            float v = lp[d * K + k];
+            int32_t t = tok[d * K + k];
+            if (isnan(v) || v > 0.0f || v == INFINITY) return 0;
+            if (k > 0 && v > lp[d * K + k - 1]) return 0;
+            if (t < 0 || t >= vocab) return 0;
+        }
+    }
+    return 1;
+}
+
+int ddto_tree_build(int B, int D, int K, int vocab, const int32_t *draft_tok,
+                    const float *draft_lp, const int32_t *root_tok, int budget, int Qc,
+                    int W, int32_t *token, int32_t *parent, int32_t *depth, int32_t *rank,
+                    float *score, int32_t *first_child, int32_t *next_sibling,
+                    uint64_t *mask, int32_t *n_nodes, int32_t *status) {
+    if (D < 1 || D > MAXD || K < 1 || budget < 1 || Qc < budget + 1 || W * 64 < Qc)
+        return -1;
+    cand_t *heap = (cand_t *)malloc(sizeof(cand_t) * (size_t)(2 * budget + 4));
+    int (*path)[MAXD] = malloc(sizeof(int[MAXD]) * (size_t)Qc);
+    for (int b = 0; b < B; ++b) {
+        const int32_t *tk = draft_tok + (size_t)b * D * K;
+        const float *lp = draft_lp + (size_t)b * D * K;
+        int32_t *o_tok = token + (size_t)b * Qc, *o_par = parent + (size_t)b * Qc;
+        int32_t *o_dep = depth + (size_t)b * Qc, *o_rank = rank + (size_t)b * Qc;
+        float *o_sc = score + (size_t)b * Qc;
+        int32_t *o_fc = first_child + (size_t)b * Qc, *o_ns = next_sibling + (size_t)b * Qc;
+        uint64_t *o_mask = mask + (size_t)b * Qc * W;
+        for (int i = 0; i < Qc; ++i) {
+            o_tok[i] = o_par[i] = o_dep[i] = o_rank[i] = o_fc[i] = o_ns[i] = -1;
+            o_sc[i] = -INFINITY;
+            for (int w = 0; w < W; ++w) o_mask[(size_t)i * W + w] = 0;
+        }
+        int ok = rows_valid(D, K, vocab, tk, lp, root_tok[b]);
+        status[b] = ok ? ORACLE_OK : ORACLE_BADINPUT;
+        /* root */
+        o_tok[0] = root_tok[b];
+        o_dep[0] = 0;
+        o_sc[0] = 0.0f;
+        o_mask[0] = 1ull;
+        int n = 1;
+        if (ok) {
+            int hn = 0;
+            cand_t c;
+            memset(&c, 0, sizeof c);
+            c.depth = 1;
+            c.ranks[0] = 0;
+            c.parent_node = 0;
+            c.score = 0.0f + lp[0];
+            heap_push(heap, &hn, &c);
+            while (n < budget + 1 && hn > 0) {
+                cand_t top = heap_pop(heap, &hn);
+                if (top.score == -INFINITY) break;
+                int i = n++;
+                int d = top.depth, r = top.ranks[d - 1];
+                o_tok[i] = tk[(d - 1) * K + r];
+                o_par[i] = top.parent_node;
+                o_dep[i] = d;
+                o_rank[i] = r;
+                o_sc[i] = top.score;
+                memcpy(path[i], top.ranks, sizeof(int) * MAXD);
+                for (int w = 0; w < W; ++w)
+                    o_mask[(size_t)i * W + w] = o_mask[(size_t)top.parent_node * W + w];
+                o_mask[(size_t)i * W + i / 64] |= 1ull << (i % 64);
+                /* next sibling: same parent, rank r+1 */
+                if (r + 1 < K) {
+                    cand_t s = top;
+                    s.ranks[d - 1] = r + 1;
+                    s.score = o_sc[top.parent_node] + lp[(d - 1) * K + r + 1];
+                    heap_push(heap, &hn, &s);
+                }
+                /* first child: depth d+1, rank 0 */
+                if (d < D) {
+                    cand_t ch = top;
+                    ch.depth = d + 1;
+                    ch.ranks[d] = 0;
+                    ch.parent_node = i;
+                    ch.score = top.score + lp[d * K + 0];
+                    heap_push(heap, &hn, &ch);
+                }
+            }
+        }
+        n_nodes[b] = n;
+        /* first child = smallest index whose parent is i; next sibling = next
+         * larger index sharing the parent */
+        for (int i = 0; i < n; ++i) {
+            for (int j = i + 1; j < n; ++j)
+                if (o_par[j] == i) { o_fc[i] = j; break; }
+            if (i > 0)
+                for (int j = i + 1; j < n; ++j)
+                    if (o_par[j] == o_par[i]) { o_ns[i] = j; break; }
+        }
+    }
+    free(heap);
+    free(path);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* attention                                                           */
+/* ------------------------------------------------------------------ */
+
+static double bf16(uint16_t v) {
+    uint32_t u = (uint32_t)v << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* One output row (b, node i, head h):
+ *   s_j  = scale * (q_lat . c_kv[j] + q_rope . k_rope[j])   for visible j
+ *   out  = sum_j softmax(s)_j c_kv[j]       (the 512-wide latent, before w_vc)
+ *   lse  = log sum_j exp(s_j)
+ * visible j: every prefix row 0..T_b-1, and row T_b+m for each m whose bit is
+ * set in the node's ancestor-or-self mask. */
+static void attn_row(int Qc, int W, int H, int Tcap, const uint16_t *q_lat,
+                     const uint16_t *q_rope, const uint16_t *c_kv, const uint16_t *k_rope,
+                     const int32_t *prefix_len, const uint64_t *mask, const int32_t *n_nodes,
+                     double scale, int b, int i, int h, double *out, double *lse,
+                     double *sbuf) {
+    if (i >= n_nodes[b]) {
+        for (int c = 0; c < 512; ++c) out[c] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    const int T = prefix_len[b];
+    const uint16_t *ql = q_lat + (((size_t)b * Qc + i) * H + h) * 512;
+    const uint16_t *qr = q_rope + (((size_t)b * Qc + i) * H + h) * 64;
+    const uint64_t *mk = mask + ((size_t)b * Qc + i) * W;
+    double ql64[512], qr64[64];
+    for (int c = 0; c < 512; ++c) ql64[c] = bf16(ql[c]);
+    for (int c = 0; c < 64; ++c) qr64[c] = bf16(qr[c]);
+    int nvis = 0;
+    int *keys = (int *)(sbuf + (T + Qc));
+    for (int j = 0; j < T; ++j) keys[nvis++] = j;
+    for (int m = 0; m < n_nodes[b]; ++m)
+        if ((mk[m / 64] >> (m % 64)) & 1ull) keys[nvis++] = T + m;
+    double mx = -INFINITY;
+    for (int v = 0; v < nvis; ++v) {
+        const uint16_t *kc = c_kv + ((size_t)b * Tcap + keys[v]) * 512;
+        const uint16_t *kr = k_rope + ((size_t)b * Tcap + keys[v]) * 64;
+        double acc = 0.0;
+        for (int c = 0; c < 512; ++c) acc += ql64[c] * bf16(kc[c]);
+        for (int c = 0; c < 64; ++c) acc += qr64[c] * bf16(kr[c]);
+        sbuf[v] = acc * scale;
+        if (sbuf[v] > mx) mx = sbuf[v];
+    }
+    double l = 0.0;
+    for (int v = 0; v < nvis; ++v) {
+        sbuf[v] = exp(sbuf[v] - mx);
+        l += sbuf[v];
+    }
+    for (int c = 0; c < 512; ++c) out[c] = 0.0;
+    for (int v = 0; v < nvis; ++v) {
+        const uint16_t *kc = c_kv + ((size_t)b * Tcap + keys[v]) * 512;
+        double p = sbuf[v] / l;
+        for (int c = 0; c < 512; ++c) out[c] += p * bf16(kc[c]);
+    }
+    *lse = mx + log(l);
+}
+
+/* rows: n_rows triples (b, i, h); out [n_rows, 512]; lse [n_rows].
+ * Returns the number of OpenMP threads used. */
+int ddto_attn_rows(int Qc, int W, int H, int Tcap, const uint16_t *q_lat,
+                   const uint16_t *q_rope, const uint16_t *c_kv, const uint16_t *k_rope,
+                   const int32_t *prefix_len, const uint64_t *mask, const int32_t *n_nodes,
+                   double scale, const int32_t *rows, long n_rows, double *out, double *lse,
+                   int n_threads) {
+    int used = 1;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel
+    {
+#pragma omp single
+        used = omp_get_num_threads();
+    }
+#endif
+    int maxT = 0;
+    long nb = 0;
+    for (long r = 0; r < n_rows; ++r) if (rows[3 * r] + 1 > nb) nb = rows[3 * r] + 1;
+    for (long b = 0; b < nb; ++b) if (prefix_len[b] > maxT) maxT = prefix_len[b];
+    size_t sb_doubles = (size_t)(maxT + Qc) * 2 + 16;
+#pragma omp parallel
+    {
+        double *sbuf = (double *)malloc(sizeof(double) * sb_doubles);
+#pragma omp for schedule(dynamic, 1)
+        for (long r = 0; r < n_rows; ++r)
+            attn_row(Qc, W, H, Tcap, q_lat, q_rope, c_kv, k_rope, prefix_len, mask, n_nodes,
+                     scale, rows[3 * r], rows[3 * r + 1], rows[3 * r + 2], out + r * 512,
+                     lse + r, sbuf);
+        free(sbuf);
+    }
+    return used;
+}
+
+/* ------------------------------------------------------------------ */
+/* greedy accept                                                       */
+/* ------------------------------------------------------------------ */
+
+/* Start at the root; while the target's argmax after the current node equals
+ * the token of one of its children, move to that child (lowest index first).
+ * accept_idx lists the visited nodes (root first), accept_len their count;
+ * commit_tok holds the accepted draft tokens followed by the bonus token (the
+ * target's argmax after the last accepted node), which is also next_root. */
+int ddto_tree_accept(int B, int D, int Qc, const int32_t *token, const int32_t *parent,
+                     const int32_t *n_nodes, const int32_t *target_argmax,
+                     int32_t *accept_len, int32_t *accept_idx, int32_t *commit_tok,
+                     int32_t *next_root) {
+    for (int b = 0; b < B; ++b) {
+        const int32_t *tk = token + (size_t)b * Qc, *pa = parent + (size_t)b * Qc;
+        const int32_t *tg = target_argmax + (size_t)b * Qc;
+        int32_t *ai = accept_idx + (size_t)b * (D + 1), *ct = commit_tok + (size_t)b * (D + 1);
+        for (int k = 0; k <= D; ++k) ai[k] = ct[k] = -1;
+        int cur = 0, len = 1;
+        ai[0] = 0;
+        for (;;) {
+            int t = tg[cur], nxt = -1;
+            for (int j = 1; j < n_nodes[b]; ++j)
+                if (pa[j] == cur && tk[j] == t) { nxt = j; break; }
+            if (nxt < 0 || len > D) break;
+            ct[len - 1] = tk[nxt];
+            ai[len++] = nxt;
+            cur = nxt;
+        }
+        ct[len - 1] = tg[cur];
+        accept_len[b] = len;
+        next_root[b] = tg[cur];
+    }
+    return 0;
+}
