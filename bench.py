@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Benchmark of the DDTree verify step (tree build -> tree-verify MLA-absorb
+attention -> greedy accept) on one GB300, against the CPU oracle.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl gb300|reference]
+
+One JSON line on stdout (rank 0). A "step" is one ddt_verify_step over the
+seeded synthetic batch of the chosen workload (default: the single-stream
+budget-8 workload, B=1 D=8 K=8 Q=9 H=64 T=4096). Inputs are resident in HBM;
+L2 is flushed (a 256 MiB write) before every timed step and every timed
+attention call, outside the timed window. The step is replayed from a CUDA
+graph and timed with CUDA events on its stream.
+
+--impl reference times the CPU oracle (the plain float64 C code) on the
+host's cores, on a bounded row sample of the same workload per step, scaled to
+a full step. Under torchrun with N>1 each rank runs an independent replica
+(the path does not shard across GPUs); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_tree_verify_ddt_gb300 import synth  # noqa: E402
+
+METRIC = "verify steps/s and verify-attn TFLOP/s (% of roofline) at 1 GB300 vs CPU oracle"
+UNIT = "verify steps/s"
+FLOP_PER_ROW_KEY = 2 * 576 + 2 * 512  # QK^T over 576 dims + PV over 512 dims
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_PEAKS["hbm_gbs"], FALLBACK_PEAKS["bf16_tflops"], "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("verify_attn.cu", "ddt_ptx.cuh"):
+        with open(os.path.join(ROOT, "mla_tree_verify_ddt_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"verify_attn_kernel_{workload_name}.txt")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not getattr(self, "out", ""):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_work(depth: np.ndarray, n_nodes: np.ndarray, prefix_len: np.ndarray, H: int):
+    """FLOP and HBM bytes one attention call must do: every valid (b, i, h)
+    row sees T_b + depth_i + 1 keys; KV rows T_b + n_b are read once per
+    sequence; Q rows in, fp32 out and lse written."""
+    flop = 0
+    byts = 0
+    for b in range(depth.shape[0]):
+        n = int(n_nodes[b])
+        T = int(prefix_len[b])
+        vis = (T + depth[b, :n].astype(np.int64) + 1).sum()
+        flop += int(vis) * H * FLOP_PER_ROW_KEY
+        byts += (T + n) * 1152 + n * H * (1152 + 2048 + 4)
+    return flop, byts
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def oracle_step_time(inp: synth.StepInputs, tree_fn, attn_budget_s: float, seed: int):
+    """Seconds for one full oracle step, measured on a bounded sample:
+    the tree build and accept run in full; attention runs on a random sample
+    of valid rows and is scaled to all rows by the per-row visible-key count."""
+    import oracle
+    wl = inp.wl
+    t0 = time.perf_counter()
+    ot = oracle.tree_build(inp.draft_tok, inp.draft_lp, inp.root_tok, wl.budget, wl.vocab)
+    t_tree = time.perf_counter() - t0
+    tg = synth.synth_target_argmax(ot.depth, ot.n_nodes, inp.draft_tok, inp.target_u,
+                                   inp.target_alt, wl.p_match)
+    t0 = time.perf_counter()
+    oracle.tree_accept(ot, tg, wl.D)
+    t_acc = time.perf_counter() - t0
+    # all valid rows and their visible-key counts
+    rows, work = [], []
+    for b in range(wl.B):
+        n = int(ot.n_nodes[b])
+        for i in range(n):
+            for h in range(wl.H):
+                rows.append((b, i, h))
+                work.append(int(inp.prefix_len[b]) + int(ot.depth[b, i]) + 1)
+    rows = np.array(rows, np.int32)
+    work = np.array(work, np.float64)
+    rng = np.random.default_rng(seed)
+    # calibrate: a small sample first, then a sample sized to the time budget
+    pick = rng.choice(len(rows), min(len(rows), 64), replace=False)
+    t0 = time.perf_counter()
+    _, _, cores = oracle.attn_rows(inp.q_lat, inp.q_rope, inp.c_kv, inp.k_rope, inp.prefix_len,
+                                   ot.mask, ot.n_nodes, inp.scale, rows[pick])
+    t_cal = time.perf_counter() - t0
+    per_key = t_cal / work[pick].sum()
+    want = max(64, min(len(rows), int(attn_budget_s / max(per_key * work.mean(), 1e-9))))
+    if want > len(pick):
+        pick = rng.choice(len(rows), want, replace=False)
+        t0 = time.perf_counter()
+        oracle.attn_rows(inp.q_lat, inp.q_rope, inp.c_kv, inp.k_rope, inp.prefix_len, ot.mask,
+                         ot.n_nodes, inp.scale, rows[pick])
+        t_s = time.perf_counter() - t0
+    else:
+        t_s = t_cal
+    t_attn = t_s * work.sum() / work[pick].sum()
+    sample = (f"tree build + accept on all {wl.B} sequences; attention on {len(pick)} of "
+              f"{len(rows)} valid (node, head) rows, scaled by visible keys")
+    return t_tree + t_acc + t_attn, cores, sample
+
+
+# ------------------------------------------------------------------ arms
+
+def reference_arm(args, wl_idx, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = synth.make_inputs(wl_idx)
+    wl = inp.wl
+    times = []
+    cores = 1
+    sample = ""
+    for s in range(args.warmup + args.steps):
+        t, cores, sample = oracle_step_time(inp, None, attn_budget_s=1.5, seed=s)
+        if s >= args.warmup:
+            times.append(t)
+    ms = 1000.0 * statistics.mean(times)
+    value = 1000.0 / ms
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(wl, inp),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(wl, inp):
+    return {"workload": wl.name, "B": wl.B, "D": wl.D, "K": wl.K, "budget": wl.budget,
+            "Q": wl.Qc, "H": wl.H, "T": list(wl.T) if isinstance(wl.T, tuple) else wl.T,
+            "Tcap": inp.Tcap, "vocab": wl.vocab, "latent": 512, "rope": 64,
+            "l2": "flushed before every timed step (256 MiB write)", "seed": synth.SEED_BASE}
+
+
+def gpu_arm(args, wl_idx, rank, world, local_rank):
+    import torch
+
+    from mla_tree_verify_ddt_gb300 import build as libbuild
+    from mla_tree_verify_ddt_gb300 import ddtree
+
+    libbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")  # host-side barrier / max only
+        pg = dist
+
+    inp = synth.make_inputs(wl_idx)
+    wl = inp.wl
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+
+    tok, lp, root = i32(inp.draft_tok), torch.from_numpy(inp.draft_lp).to(dev), i32(inp.root_tok)
+    q_lat, q_rope, c_kv, k_rope = bf16(inp.q_lat), bf16(inp.q_rope), bf16(inp.c_kv), bf16(inp.k_rope)
+    pl = i32(inp.prefix_len)
+    # target argmax of the synthetic target model needs the tree: build it
+    # once on the device, outside any timed region
+    tree0 = ddtree.ddt_tree_build(tok, lp, root, wl.budget, wl.vocab)
+    depth = tree0.depth.cpu().numpy()
+    n_nodes = tree0.n_nodes.cpu().numpy()
+    tg = i32(synth.synth_target_argmax(depth, n_nodes, inp.draft_tok, inp.target_u,
+                                       inp.target_alt, wl.p_match))
+    step = ddtree.VerifyStep(tok, lp, root, wl.vocab, wl.budget, q_lat, q_rope, c_kv, k_rope, pl,
+                             tg, inp.scale)
+    plan_nsplit = step.ws_bytes and (step.ws_bytes // (wl.B * wl.Qc * wl.H * 513 * 4)) or 1
+    launches_per_step = 3 + (1 if plan_nsplit > 1 else 0)
+
+    s = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(s):
+        step.run(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step.run(s)
+    # attention alone (the dominant kernel), also as a graph
+    attn_out = torch.empty_like(step.out)
+    attn_lse = torch.empty_like(step.lse)
+    with torch.cuda.stream(s):
+        ddtree.ddt_verify_mla_attn(q_lat, q_rope, c_kv, k_rope, pl, step.tree, inp.scale,
+                                   attn_out, attn_lse, step.workspace, stream=s)
+    torch.cuda.synchronize()
+    ga = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ga, stream=s):
+        ddtree.ddt_verify_mla_attn(q_lat, q_rope, c_kv, k_rope, pl, step.tree, inp.scale,
+                                   attn_out, attn_lse, step.workspace, stream=s)
+
+    def timed(graph, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        with torch.cuda.stream(s):
+            for e0, e1 in evs:
+                flush.fill_(1)          # evict L2, outside the timed window
+                e0.record(s)
+                graph.replay()
+                e1.record(s)
+        return evs
+
+    # warm-up
+    for e0, e1 in timed(g, args.warmup):
+        pass
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph-replayed steps
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        evs = timed(g, args.steps)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms = sum(step_ms)
+    if pg:
+        t = torch.tensor([total_ms])
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * 1000.0 / ms_per_step
+
+    # ---- dominant kernel: attention alone, same protocol
+    for _ in timed(ga, 3):
+        pass
+    torch.cuda.synchronize()
+    aevs = timed(ga, max(args.steps, 10))
+    torch.cuda.synchronize()
+    attn_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in aevs)
+    flop, algo_bytes = algorithmic_work(depth, n_nodes, inp.prefix_len, wl.H)
+    hbm_gbs, bf16_tflops, peak_src = load_peaks()
+    t_tensor = flop / (bf16_tflops * 1e12)
+    t_hbm = algo_bytes / (hbm_gbs * 1e9)
+    attn_s = attn_ms / 1e3
+    if t_tensor >= t_hbm:
+        roof = {"bound": "tensor", "achieved": flop / attn_s / 1e12, "peak": bf16_tflops,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": algo_bytes / attn_s / 1e9, "peak": hbm_gbs,
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = profiled_traffic(wl.name)
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else peak_src
+    roof["kernel"] = "verify_attn_kernel (+ merge_chunks_kernel when the key range is split)"
+    roof["algorithmic_flop_per_launch"] = flop
+    roof["algorithmic_bytes_per_launch"] = algo_bytes
+    roof["launch_ms"] = attn_ms
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_tok, h_lp, h_root = pin(inp.draft_tok), pin(inp.draft_lp), pin(inp.root_tok)
+    h_ql = pin(inp.q_lat.view(np.int16))
+    h_qr = pin(inp.q_rope.view(np.int16))
+    h_tg = pin(tg.cpu().numpy())
+    h_pl = pin(inp.prefix_len)
+    node_rows = [(b, int(inp.prefix_len[b])) for b in range(wl.B)]
+    h_ckv_nodes = [pin(inp.c_kv[b, T:T + wl.Qc].view(np.int16)) for b, T in node_rows]
+    h_kr_nodes = [pin(inp.k_rope[b, T:T + wl.Qc].view(np.int16)) for b, T in node_rows]
+    o_len = torch.empty(wl.B, dtype=torch.int32).pin_memory()
+    o_tok = torch.empty(wl.B, wl.D + 1, dtype=torch.int32).pin_memory()
+    o_root = torch.empty(wl.B, dtype=torch.int32).pin_memory()
+    ql16, qr16 = q_lat.view(torch.int16), q_rope.view(torch.int16)
+    ckv16, kr16 = c_kv.view(torch.int16), k_rope.view(torch.int16)
+    h2d = sum(t.numel() * t.element_size() for t in
+              [h_tok, h_lp, h_root, h_ql, h_qr, h_tg, h_pl, *h_ckv_nodes, *h_kr_nodes])
+    d2h = sum(t.numel() * t.element_size() for t in (o_len, o_tok, o_root))
+
+    def e2e_step():
+        tok.copy_(h_tok, non_blocking=True)
+        lp.copy_(h_lp, non_blocking=True)
+        root.copy_(h_root, non_blocking=True)
+        ql16.copy_(h_ql, non_blocking=True)
+        qr16.copy_(h_qr, non_blocking=True)
+        tg.copy_(h_tg, non_blocking=True)
+        pl.copy_(h_pl, non_blocking=True)
+        for (b, T), hc, hk in zip(node_rows, h_ckv_nodes, h_kr_nodes):
+            ckv16[b, T:T + wl.Qc].copy_(hc, non_blocking=True)
+            kr16[b, T:T + wl.Qc].copy_(hk, non_blocking=True)
+        step.run(s)
+        o_len.copy_(step.acc.accept_len, non_blocking=True)
+        o_tok.copy_(step.acc.commit_tok, non_blocking=True)
+        o_root.copy_(step.acc.next_root, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    with torch.cuda.stream(s):
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            e2e_step()
+            e1.record(s)
+            e1.synchronize()  # the host needs the accept result before the next step
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_value = world * 1000.0 / statistics.mean(e2e_ms)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**config_dict(wl, inp), "graph": True, "key_range_splits": plan_nsplit,
+                   "sequences_per_s": value * wl.B,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "attn_tflops": flop / attn_s / 1e12,
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        t, cores, sample = oracle_step_time(inp, None, attn_budget_s=12.0, seed=1)
+        line["cpu_baseline"] = {"value": 1.0 / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=1, help="index into synth.WORKLOADS")
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, args.workload, rank, world)
+    else:
+        gpu_arm(args, args.workload, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,37 @@
+// Internal launch interfaces between the C-ABI layer (ddt_api.cu) and the
+// kernels. Not installed; the public contract is include/ddtree.h.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ddtree.h"
+
+namespace ddt {
+
+// Bounded-wait limit for every on-chip wait of the attention kernel.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+cudaError_t launch_tree_build(const ddt_draft &in, int budget, const ddt_tree &out,
+                              cudaStream_t s);
+cudaError_t launch_tree_accept(const ddt_tree &tree, const int32_t *target,
+                               const ddt_accept &out, cudaStream_t s);
+
+struct AttnPlan {
+    int mtiles;       // 128-row tiles of Qc*H rows per sequence
+    int nsplit;       // key-range chunks per (sequence, row tile)
+    size_t ws_bytes;  // partial outputs when nsplit > 1
+};
+
+// Geometry for one attention call on a device with `sms` multiprocessors.
+AttnPlan plan_attention(int B, int Qc, int H, int Tcap, int sms);
+
+// Encodes the tensor maps and enqueues the attention kernel (and the merge
+// kernel when nsplit > 1).
+int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
+                       const ddt_attn_out &out, void *workspace, size_t ws_bytes,
+                       const AttnPlan &plan, cudaStream_t s);
+
+cudaError_t launch_selftest_wait(int32_t *status, unsigned timeout_us, cudaStream_t s);
+
+}  // namespace ddt

@@ -1,0 +1,278 @@
+"""ctypes binding for libddtree (include/ddtree.h).
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+kernels of libddtree.so. PyTorch provides device memory and streams. If the
+library is missing this module raises at import-time use; there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libddtree.so")
+
+DDT_OK, DDT_E_INVAL, DDT_E_CUDA, DDT_E_UNSUPPORTED, DDT_E_BADINPUT, DDT_E_TIMEOUT = range(6)
+MAX_DEPTH, MAX_TOPK, MAX_BUDGET, LATENT, ROPE = 16, 16, 64, 512, 64
+
+EXPORTED = ["ddt_workspace_size", "ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept",
+            "ddt_verify_step", "ddt_status_str", "ddt_read_device_status",
+            "ddt_selftest_bounded_wait"]
+
+P = ctypes.c_void_p
+I = ctypes.c_int
+
+
+class DdtDraft(ctypes.Structure):
+    _fields_ = [("B", I), ("D", I), ("K", I), ("vocab", I), ("tok", P), ("lp", P), ("root_tok", P)]
+
+
+class DdtTree(ctypes.Structure):
+    _fields_ = [("B", I), ("D", I), ("Qc", I), ("W", I), ("token", P), ("parent", P), ("depth", P),
+                ("rank", P), ("score", P), ("first_child", P), ("next_sibling", P), ("mask", P),
+                ("n_nodes", P), ("status", P)]
+
+
+class DdtAttnIn(ctypes.Structure):
+    _fields_ = [("H", I), ("Tcap", I), ("q_lat", P), ("q_rope", P), ("c_kv", P), ("k_rope", P),
+                ("prefix_len", P)]
+
+
+class DdtAttnOut(ctypes.Structure):
+    _fields_ = [("out", P), ("lse", P)]
+
+
+class DdtAccept(ctypes.Structure):
+    _fields_ = [("accept_len", P), ("accept_idx", P), ("commit_tok", P), ("next_root", P)]
+
+
+class DdtError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_str(code)} ({code})")
+        self.code = code
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libddtree.so (built by mla_tree_verify_ddt_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libddtree.so is not built ({LIB_PATH}); run "
+                               "python -m mla_tree_verify_ddt_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        L.ddt_workspace_size.argtypes = [I, I, I, I, I, I]
+        L.ddt_workspace_size.restype = ctypes.c_size_t
+        L.ddt_tree_build.argtypes = [ctypes.POINTER(DdtDraft), I, ctypes.POINTER(DdtTree), P]
+        L.ddt_verify_mla_attn.argtypes = [ctypes.POINTER(DdtAttnIn), ctypes.POINTER(DdtTree),
+                                          ctypes.c_float, ctypes.POINTER(DdtAttnOut), P,
+                                          ctypes.c_size_t, P]
+        L.ddt_tree_accept.argtypes = [ctypes.POINTER(DdtTree), P, ctypes.POINTER(DdtAccept), P]
+        L.ddt_verify_step.argtypes = [ctypes.POINTER(DdtDraft), I, ctypes.POINTER(DdtTree),
+                                      ctypes.POINTER(DdtAttnIn), ctypes.c_float,
+                                      ctypes.POINTER(DdtAttnOut), P, ctypes.POINTER(DdtAccept), P,
+                                      ctypes.c_size_t, P]
+        L.ddt_status_str.argtypes = [I]
+        L.ddt_status_str.restype = ctypes.c_char_p
+        L.ddt_read_device_status.argtypes = [P, I, P]
+        L.ddt_selftest_bounded_wait.argtypes = [P, ctypes.c_uint, P]
+        for f in ("ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept", "ddt_verify_step",
+                  "ddt_read_device_status", "ddt_selftest_bounded_wait"):
+            getattr(L, f).restype = I
+        _lib = L
+    return _lib
+
+
+def status_str(code: int) -> str:
+    return lib().ddt_status_str(int(code)).decode()
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(rc: int, what: str):
+    if rc != DDT_OK:
+        raise DdtError(rc, what)
+
+
+# ------------------------------------------------------------------ buffers
+
+@dataclass
+class Tree:
+    """Device tensors of one built tree batch (shapes as in ddtree.h)."""
+    B: int
+    D: int
+    Qc: int
+    W: int
+    token: torch.Tensor
+    parent: torch.Tensor
+    depth: torch.Tensor
+    rank: torch.Tensor
+    score: torch.Tensor
+    first_child: torch.Tensor
+    next_sibling: torch.Tensor
+    mask: torch.Tensor          # int64 view of the uint64 words
+    n_nodes: torch.Tensor
+    status: torch.Tensor
+
+    @staticmethod
+    def empty(B: int, D: int, budget: int, device="cuda") -> "Tree":
+        Qc = budget + 1
+        W = (Qc + 63) // 64
+        i32 = dict(dtype=torch.int32, device=device)
+        return Tree(B, D, Qc, W, *[torch.empty(B, Qc, **i32) for _ in range(4)],
+                    torch.empty(B, Qc, dtype=torch.float32, device=device),
+                    torch.empty(B, Qc, **i32), torch.empty(B, Qc, **i32),
+                    torch.empty(B, Qc, W, dtype=torch.int64, device=device),
+                    torch.empty(B, **i32), torch.empty(B, **i32))
+
+    def c(self) -> DdtTree:
+        return DdtTree(self.B, self.D, self.Qc, self.W, *[_ptr(getattr(self, f)) for f in
+                       ("token", "parent", "depth", "rank", "score", "first_child",
+                        "next_sibling", "mask", "n_nodes", "status")])
+
+
+@dataclass
+class Accept:
+    accept_len: torch.Tensor
+    accept_idx: torch.Tensor
+    commit_tok: torch.Tensor
+    next_root: torch.Tensor
+
+    @staticmethod
+    def empty(B: int, D: int, device="cuda") -> "Accept":
+        i32 = dict(dtype=torch.int32, device=device)
+        return Accept(torch.empty(B, **i32), torch.empty(B, D + 1, **i32),
+                      torch.empty(B, D + 1, **i32), torch.empty(B, **i32))
+
+    def c(self) -> DdtAccept:
+        return DdtAccept(_ptr(self.accept_len), _ptr(self.accept_idx), _ptr(self.commit_tok),
+                         _ptr(self.next_root))
+
+
+def draft_struct(tok, lp, root_tok, vocab: int) -> DdtDraft:
+    B, D, K = tok.shape
+    return DdtDraft(B, D, K, vocab, _ptr(tok), _ptr(lp), _ptr(root_tok))
+
+
+def attn_in_struct(q_lat, q_rope, c_kv, k_rope, prefix_len) -> DdtAttnIn:
+    return DdtAttnIn(q_lat.shape[2], c_kv.shape[1], _ptr(q_lat), _ptr(q_rope), _ptr(c_kv),
+                     _ptr(k_rope), _ptr(prefix_len))
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("libddtree takes dense row-major tensors")
+
+
+# ------------------------------------------------------------------ calls
+
+def ddt_workspace_size(B: int, D: int, K: int, budget: int, H: int, Tcap: int) -> int:
+    return int(lib().ddt_workspace_size(B, D, K, budget, H, Tcap))
+
+
+def ddt_tree_build(tok, lp, root_tok, budget: int, vocab: int, out: Tree | None = None,
+                   stream=None) -> Tree:
+    _contig(tok, lp, root_tok)
+    B, D, _ = tok.shape
+    out = out or Tree.empty(B, D, budget, tok.device)
+    d, t = draft_struct(tok, lp, root_tok, vocab), out.c()
+    _check(lib().ddt_tree_build(ctypes.byref(d), budget, ctypes.byref(t), _stream_ptr(stream)),
+           "ddt_tree_build")
+    return out
+
+
+def ddt_verify_mla_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: Tree, scale: float,
+                        out=None, lse=None, workspace=None, stream=None):
+    _contig(q_lat, q_rope, c_kv, k_rope, prefix_len)
+    B, Qc, H, _ = q_lat.shape
+    if out is None:
+        out = torch.empty(B, Qc, H, LATENT, dtype=torch.float32, device=q_lat.device)
+    if lse is None:
+        lse = torch.empty(B, Qc, H, dtype=torch.float32, device=q_lat.device)
+    ws = ddt_workspace_size(B, tree.D, 1, Qc - 1, H, c_kv.shape[1])
+    if workspace is None and ws:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=q_lat.device)
+    a = attn_in_struct(q_lat, q_rope, c_kv, k_rope, prefix_len)
+    o = DdtAttnOut(_ptr(out), _ptr(lse))
+    t = tree.c()
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().ddt_verify_mla_attn(ctypes.byref(a), ctypes.byref(t), float(scale),
+                                     ctypes.byref(o), _ptr(workspace), wsb, _stream_ptr(stream)),
+           "ddt_verify_mla_attn")
+    return out, lse
+
+
+def ddt_tree_accept(tree: Tree, target_argmax, out: Accept | None = None, stream=None) -> Accept:
+    _contig(target_argmax)
+    out = out or Accept.empty(tree.B, tree.D, target_argmax.device)
+    t, a = tree.c(), out.c()
+    _check(lib().ddt_tree_accept(ctypes.byref(t), _ptr(target_argmax), ctypes.byref(a),
+                                 _stream_ptr(stream)), "ddt_tree_accept")
+    return out
+
+
+class VerifyStep:
+    """All buffers of one ddt_verify_step call, allocated once.
+
+    ``run()`` enqueues the whole step (build -> attention -> merge -> accept)
+    through the single C-ABI call, with the marshalled structs prebuilt so a
+    call costs one ctypes transition.
+    """
+
+    def __init__(self, tok, lp, root_tok, vocab: int, budget: int, q_lat, q_rope, c_kv, k_rope,
+                 prefix_len, target_argmax, scale: float):
+        _contig(tok, lp, root_tok, q_lat, q_rope, c_kv, k_rope, prefix_len, target_argmax)
+        dev = tok.device
+        B, D, K = tok.shape
+        H = q_lat.shape[2]
+        self.inputs = (tok, lp, root_tok, q_lat, q_rope, c_kv, k_rope, prefix_len, target_argmax)
+        self.tree = Tree.empty(B, D, budget, dev)
+        self.acc = Accept.empty(B, D, dev)
+        self.out = torch.empty(B, budget + 1, H, LATENT, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(B, budget + 1, H, dtype=torch.float32, device=dev)
+        self.ws_bytes = ddt_workspace_size(B, D, K, budget, H, c_kv.shape[1])
+        self.workspace = torch.empty(max(self.ws_bytes, 1), dtype=torch.uint8, device=dev)
+        self.budget = budget
+        self.scale = float(scale)
+        self._d = draft_struct(tok, lp, root_tok, vocab)
+        self._t = self.tree.c()
+        self._a = attn_in_struct(q_lat, q_rope, c_kv, k_rope, prefix_len)
+        self._o = DdtAttnOut(_ptr(self.out), _ptr(self.lse))
+        self._c = self.acc.c()
+        self._tg = _ptr(target_argmax)
+
+    def run(self, stream=None):
+        rc = lib().ddt_verify_step(ctypes.byref(self._d), self.budget, ctypes.byref(self._t),
+                                   ctypes.byref(self._a), self.scale, ctypes.byref(self._o),
+                                   self._tg, ctypes.byref(self._c), _ptr(self.workspace),
+                                   self.ws_bytes, _stream_ptr(stream))
+        _check(rc, "ddt_verify_step")
+
+
+def ddt_read_device_status(status: torch.Tensor):
+    import numpy as np
+    host = np.empty(status.numel(), np.int32)
+    _check(lib().ddt_read_device_status(_ptr(status), status.numel(),
+                                        host.ctypes.data_as(ctypes.c_void_p)),
+           "ddt_read_device_status")
+    return host
+
+
+def ddt_selftest_bounded_wait(status: torch.Tensor, timeout_us: int, stream=None):
+    _check(lib().ddt_selftest_bounded_wait(_ptr(status), int(timeout_us), _stream_ptr(stream)),
+           "ddt_selftest_bounded_wait")

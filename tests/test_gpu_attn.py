@@ -1,0 +1,139 @@
+"""GPU tree-verify attention vs the float64 oracle.
+
+Small cases are compared on every row; the large workloads, in the launch
+configuration the benchmark times, on sampled rows the oracle computes one
+by one. Tolerance: max-abs 2e-3 and rel 1e-2 per element (gpu_util)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_tree_verify_ddt_gb300 import ddtree, synth
+from tests import gpu_util as gu
+from tests.test_oracle_tree import random_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ddtree.lib()
+    torch.cuda.init()
+
+
+def run_attn(inp, gt=None):
+    wl = inp.wl
+    if gt is None:
+        gt = ddtree.ddt_tree_build(gu.i32_dev(inp.draft_tok), gu.f32_dev(inp.draft_lp),
+                                   gu.i32_dev(inp.root_tok), wl.budget, wl.vocab)
+    q_lat, q_rope, c_kv, k_rope, pl = gu.attn_dev(inp)
+    out, lse = ddtree.ddt_verify_mla_attn(q_lat, q_rope, c_kv, k_rope, pl, gt, inp.scale)
+    torch.cuda.synchronize()
+    return gt, out.cpu().numpy(), lse.cpu().numpy()
+
+
+def custom_inputs(seed, B, D, K, budget, H, T, tail="nan", underfull=0, vocab=4000):
+    wl = synth.Workload(f"custom{seed}", B, D, K, budget, H, 0, vocab, 0.7, underfull)
+    rng = np.random.default_rng(seed)
+    tok, lp = random_rows(rng, B, D, K, vocab=vocab)
+    for b in range(underfull):
+        lp[b] = -np.inf
+        lp[b, :, 0] = 0.0
+    T = np.asarray(T, np.int32)
+    Tcap = int(T.max()) + wl.Qc + 5
+    inp = synth.StepInputs(
+        wl, tok, lp, rng.integers(0, vocab, B).astype(np.int32), T, Tcap,
+        synth.normal_bf16(rng, (B, wl.Qc, H, 512)), synth.normal_bf16(rng, (B, wl.Qc, H, 64)),
+        synth.normal_bf16(rng, (B, Tcap, 512)), synth.normal_bf16(rng, (B, Tcap, 64)),
+        rng.random((B, wl.Qc)), rng.integers(0, vocab, (B, wl.Qc)).astype(np.int32),
+        synth.SOFTMAX_SCALE)
+    return inp
+
+
+def nan_tail(inp, ot):
+    """Fill every KV row no node may see (past T_b + n_nodes) and every padded
+    query row with NaN: none of it may reach an output."""
+    for b in range(inp.wl.B):
+        lo = int(inp.prefix_len[b]) + int(ot.n_nodes[b])
+        inp.c_kv[b, lo:] = 0x7FC0
+        inp.k_rope[b, lo:] = 0x7FC0
+        inp.q_lat[b, int(ot.n_nodes[b]):] = 0x7FC0
+        inp.q_rope[b, int(ot.n_nodes[b]):] = 0x7FC0
+
+
+def full_check(inp, what):
+    ot = gu.oracle_tree(inp)
+    nan_tail(inp, ot)
+    gt, out, lse = run_attn(inp)
+    gu.assert_tree_equal(gt, ot)
+    ref_out, ref_lse = oracle.attn_all(inp.q_lat, inp.q_rope, inp.c_kv, inp.k_rope,
+                                       inp.prefix_len, ot.mask, ot.n_nodes, inp.scale)
+    err = gu.check_rows(out, lse, ref_out, ref_lse, what)
+    return err
+
+
+@pytest.mark.parametrize("idx", [0, 1])
+def test_full_parity_small_workloads(idx):
+    err = full_check(synth.make_inputs(idx), synth.WORKLOADS[idx].name)
+    print(f"max abs err {err:.3e}")
+
+
+@pytest.mark.parametrize("seed,B,D,K,budget,H,T,underfull", [
+    (1, 3, 5, 4, 20, 8, [0, 37, 300], 0),        # 2 row tiles, ragged prefixes, T=0
+    (2, 2, 16, 8, 64, 2, [129, 64], 0),          # W=2 masks, node keys across tiles
+    (3, 4, 15, 4, 32, 5, [1, 63, 64, 65], 1),    # odd H, tile-edge prefixes, a chain
+    (4, 1, 1, 1, 1, 1, [0], 0),                  # budget 1, H 1, no prefix
+    (5, 2, 8, 8, 16, 64, [500, 1337], 0),        # H 64: rows = 2 nodes per tile
+    (6, 1, 4, 4, 8, 130, [70], 0),               # H > 128: a node spans tiles
+])
+def test_full_parity_custom(seed, B, D, K, budget, H, T, underfull):
+    inp = custom_inputs(seed, B, D, K, budget, H, T, underfull=underfull)
+    full_check(inp, f"custom seed {seed}")
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4])
+def test_sampled_parity_large_workloads(idx):
+    inp = synth.make_inputs(idx)
+    wl = inp.wl
+    ot = gu.oracle_tree(inp)
+    gt, out, lse = run_attn(inp)
+    gu.assert_tree_equal(gt, ot)
+    heads = 3 if idx != 4 else 1
+    rows = gu.sample_rows(wl.B, wl.Qc, wl.H, ot.n_nodes, seed=idx, per_seq_heads=heads,
+                          max_seqs=8 if idx != 4 else 4)
+    ref_out, ref_lse = gu.oracle_rows(inp, ot, rows)
+    got_out = out[rows[:, 0], rows[:, 1], rows[:, 2]]
+    got_lse = lse[rows[:, 0], rows[:, 1], rows[:, 2]]
+    err = gu.check_rows(got_out, got_lse, ref_out, ref_lse, wl.name)
+    print(f"{wl.name}: {len(rows)} rows, max abs err {err:.3e}")
+    # properties at full size: padded rows are exactly zero; all else finite
+    for b in range(wl.B):
+        n = int(ot.n_nodes[b])
+        assert np.all(out[b, n:] == 0) and np.all(lse[b, n:] == -np.inf)
+        assert np.all(np.isfinite(out[b, :n])) and np.all(np.isfinite(lse[b, :n]))
+
+
+def test_prefix_out_of_range_is_flagged():
+    inp = custom_inputs(9, 3, 4, 4, 8, 4, [10, 10, 10])
+    inp.prefix_len[1] = inp.Tcap - 2  # T + n_nodes > Tcap
+    gt, out, lse = run_attn(inp)
+    st = ddtree.ddt_read_device_status(gt.status)
+    assert list(st) == [ddtree.DDT_OK, ddtree.DDT_E_BADINPUT, ddtree.DDT_OK]
+    assert np.all(out[1] == 0) and np.all(lse[1] == -np.inf)
+    assert np.all(np.isfinite(out[0, :9])) and np.all(np.isfinite(out[2, :9]))
+
+
+def test_root_only_tree_without_prefix_is_its_own_row():
+    """T = 0 and a chain budget of 1 with a -inf drafter: node 0 sees only
+    its own key, so out is that key's latent exactly."""
+    inp = custom_inputs(10, 2, 3, 2, 4, 3, [0, 0])
+    inp.draft_lp[:] = -np.inf
+    ot = gu.oracle_tree(inp)
+    assert (ot.n_nodes == 1).all()
+    gt, out, lse = run_attn(inp)
+    for b in range(2):
+        row = synth.bf16_bits_to_f64(inp.c_kv[b, 0]).astype(np.float32)
+        for h in range(3):
+            np.testing.assert_array_equal(out[b, 0, h], row)
