@@ -28,14 +28,19 @@
 //    live in tensor memory and feed the MMA as its A operand;
 //  * KV arrives by TMA in 64-column chunks: the four chunks that are this
 //    half's V are double-buffered per tile and serve both S and PV; the other
-//    five chunks stream through a 4-slot ring;
+//    five chunks stream through a 4-slot ring fed by a second producer warp,
+//    so ring loads never queue behind V loads. S consumes the streamed chunks
+//    first and the V chunks last, and a ready PV is slipped in between S
+//    chunks;
 //  * softmax runs on 4 warps, one thread per row, in fp32 in the log2 domain,
 //    with a lazily moved reference max (O is rescaled only when a row's max
 //    grows by more than 2^8);
 //  * PV runs in fp16 (P rounded to fp16, 2^-11 relative, four times tighter
 //    than bf16): after S of a tile has read its V chunks as bf16 K, the
-//    softmax warps convert those chunks to fp16 in place. The row sum
-//    accumulates the rounded P the product consumes;
+//    softmax warps convert those chunks to fp16 in place;
+//  * the softmax code is kept compact (visibility as one 64-bit word per
+//    tile, rolled loops off the per-key path): the fully unrolled version
+//    spent most of its time waiting for instruction fetch;
 //  * when the key range is split over several CTAs, each writes a normalised
 //    partial and its lse; a second kernel merges them.
 // Every mbarrier wait is bounded; on expiry the CTA records DDT_E_TIMEOUT in
@@ -78,6 +83,8 @@ constexpr uint32_t kColQR = 448;  // 32: rotary query (bf16 pairs)
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// warps 0-3 softmax/epilogue, 4 TMA (Q, V), 5 MMA, 6 TMA (streamed chunks)
+constexpr int kThreads = 224;
 
 // barrier indices
 enum {
@@ -110,15 +117,28 @@ struct AttnArgs {
     unsigned long long wait_ns;
 };
 
-__device__ __forceinline__ bool key_visible(int key, int T, int n, uint64_t m0, uint64_t m1) {
-    if (key < T) return true;
-    const int m = key - T;
-    if (m >= n) return false;
-    const uint64_t w = (m < 64) ? m0 : m1;
-    return (w >> (m & 63)) & 1ull;
+// Visibility of keys key0..key0+63 for a node with ancestor mask (m0, m1):
+// every prefix key (< T) and the keys T+m of ancestors-or-self m < n. Only
+// tiles that reach past the prefix need it; the loop stays rolled to keep
+// the softmax code small.
+__device__ __noinline__ uint64_t tile_visibility(int key0, int T, int n, uint64_t m0, uint64_t m1) {
+    uint64_t vis = 0;
+#pragma unroll 1
+    for (int k = 0; k < 64; ++k) {
+        const int key = key0 + k;
+        bool v;
+        if (key < T) {
+            v = true;
+        } else {
+            const int m = key - T;
+            v = m < n && (((m < 64 ? m0 : m1) >> (m & 63)) & 1ull);
+        }
+        vis |= static_cast<uint64_t>(v) << k;
+    }
+    return vis;
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     verify_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_kv,
                        const __grid_constant__ CUtensorMap tm_kr, const AttnArgs a) {
@@ -205,19 +225,17 @@ __global__ void __launch_bounds__(192, 1)
     };
 
     if (warp == 4) {
-        // ======================= TMA producer =======================
+        // ================= TMA producer: Q once, then this half's V chunks =================
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_kv);
-            tma_prefetch_desc(&tm_kr);
             const int qrow = static_cast<int>(row_base) + mt * kRows;
             mbar_arrive_expect_tx(bar(BAR_Q_FULL), kQChunks * kChunkBytesQ);
             for (int c = 0; c < kQChunks; ++c)
                 tma_load_2d(sQ + c * kChunkBytesQ, &tm_q, c * 64, qrow, bar(BAR_Q_FULL));
-            int armed_v[2] = {0, 0}, armed_st[kStreamSlots] = {0, 0, 0, 0};
-            int st_cnt = 0;
+            int armed_v[2] = {0, 0};
             bool ok = true;
-            for (int jj = 0; jj < nt && ok; ++jj) {
+            for (int jj = 0; jj < nt; ++jj) {
                 const int key_row = b * a.Tcap + (t0 + jj) * kKeys;
                 const int vs = jj & 1;
                 if (jj >= 2 && !mbar_wait(bar(BAR_V_EMPTY + vs), ((jj - 2) >> 1) & 1, deadline, abort_flag)) {
@@ -229,6 +247,26 @@ __global__ void __launch_bounds__(192, 1)
                 for (int c = 0; c < kVChunks; ++c)
                     tma_load_2d(sV + vs * kVSetBytes + c * kChunkBytesKV, &tm_kv,
                                 (kVChunks * half + c) * 64, key_row, bar(BAR_V_FULL + vs));
+            }
+            if (!ok) {
+                fail();
+                // let every copy this thread started land before the CTA leaves
+                const uint64_t drain_deadline = globaltimer_ns() + 100000000ull;
+                const int zero = 0;
+                mbar_wait(bar(BAR_Q_FULL), 0, drain_deadline, &zero);
+                for (int s = 0; s < 2; ++s)
+                    if (armed_v[s]) mbar_wait(bar(BAR_V_FULL + s), (armed_v[s] - 1) & 1, drain_deadline, &zero);
+            }
+        }
+    } else if (warp == 6) {
+        // ====== TMA producer: the other latent half and the rotary key, through the ring ======
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_kr);
+            int armed_st[kStreamSlots] = {0, 0, 0, 0};
+            int st_cnt = 0;
+            bool ok = true;
+            for (int jj = 0; jj < nt && ok; ++jj) {
+                const int key_row = b * a.Tcap + (t0 + jj) * kKeys;
                 for (int q = 0; q < kStreamPerTile; ++q) {
                     const int slot = st_cnt % kStreamSlots, use = st_cnt / kStreamSlots;
                     if (use >= 1 && !mbar_wait(bar(BAR_ST_EMPTY + slot), (use - 1) & 1, deadline, abort_flag)) {
@@ -248,12 +286,8 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (!ok) {
                 fail();
-                // let every copy this thread started land before the CTA leaves
                 const uint64_t drain_deadline = globaltimer_ns() + 100000000ull;
                 const int zero = 0;
-                mbar_wait(bar(BAR_Q_FULL), 0, drain_deadline, &zero);
-                for (int s = 0; s < 2; ++s)
-                    if (armed_v[s]) mbar_wait(bar(BAR_V_FULL + s), (armed_v[s] - 1) & 1, drain_deadline, &zero);
                 for (int s = 0; s < kStreamSlots; ++s)
                     if (armed_st[s]) mbar_wait(bar(BAR_ST_FULL + s), (armed_st[s] - 1) & 1, drain_deadline, &zero);
             }
@@ -267,9 +301,17 @@ __global__ void __launch_bounds__(192, 1)
                       mbar_wait(bar(BAR_QR_READY), 0, deadline, abort_flag);
             tc_fence_after();
             int st_cnt = 0;
-            auto issue_pv = [&](int j) -> bool {
+            int pv_next = 0;  // the next tile whose PV is still to be issued
+            // O += P_j V_j once the softmax has published P_j. With block ==
+            // false it only issues when P_j is already there, so a PV can slip
+            // in between the chunks of the next S as soon as it is ready.
+            auto issue_pv = [&](int j, bool block) -> int {
                 const int pb = j & 1;
-                if (!mbar_wait(bar(BAR_P_FULL + pb), (j >> 1) & 1, deadline, abort_flag)) return false;
+                if (block) {
+                    if (!mbar_wait(bar(BAR_P_FULL + pb), (j >> 1) & 1, deadline, abort_flag)) return -1;
+                } else if (!mbar_try_wait(bar(BAR_P_FULL + pb), (j >> 1) & 1)) {
+                    return 0;
+                }
                 tc_fence_after();
                 const uint32_t vb = sV + pb * kVSetBytes;
                 for (int ks = 0; ks < kKeys / 16; ++ks)
@@ -278,7 +320,7 @@ __global__ void __launch_bounds__(192, 1)
                            (j > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(bar(BAR_PV_DONE + pb));
                 mma_commit(bar(BAR_V_EMPTY + pb));
-                return true;
+                return 1;
             };
             for (int jj = 0; jj < nt && ok; ++jj) {
                 const int sb = jj & 1;
@@ -286,24 +328,8 @@ __global__ void __launch_bounds__(192, 1)
                     ok = false;
                     break;
                 }
-                if (!mbar_wait(bar(BAR_V_FULL + sb), (jj >> 1) & 1, deadline, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
                 const uint32_t dS = tmem + kColS + sb * kKeys;
-                uint32_t acc = 0;
-                // this half's latent columns: the V chunks double as K
-                for (int c = 0; c < kVChunks; ++c) {
-                    const uint32_t qa = sQ + (kVChunks * half + c) * kChunkBytesQ;
-                    const uint32_t kb = sV + sb * kVSetBytes + c * kChunkBytesKV;
-                    for (int ks = 0; ks < 4; ++ks) {
-                        mma_ss(dS, desc_sw128(qa + ks * 32, 16, 1024), desc_sw128(kb + ks * 32, 16, 1024),
-                               idS, acc);
-                        acc = 1;
-                    }
-                }
-                // the other latent half and the rotary part, streamed
+                // the streamed chunks first: the other latent half and the rotary part
                 for (int q = 0; q < kStreamPerTile; ++q) {
                     const int slot = st_cnt % kStreamSlots, use = st_cnt / kStreamSlots;
                     if (!mbar_wait(bar(BAR_ST_FULL + slot), use & 1, deadline, abort_flag)) {
@@ -315,23 +341,43 @@ __global__ void __launch_bounds__(192, 1)
                     if (q < 4) {
                         const uint32_t qa = sQ + (kVChunks * (1 - half) + q) * kChunkBytesQ;
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(dS, desc_sw128(qa + ks * 32, 16, 1024),
-                                   desc_sw128(kb + ks * 32, 16, 1024), idS, 1u);
+                            mma_ss(dS, desc_sw128(qa + ks * 32, 16, 1024), desc_sw128(kb + ks * 32, 16, 1024),
+                                   idS, (q > 0 || ks > 0) ? 1u : 0u);
                     } else {
                         for (int ks = 0; ks < 4; ++ks)
                             mma_ts(dS, tmem + kColQR + ks * 8, desc_sw128(kb + ks * 32, 16, 1024), idS, 1u);
                     }
                     mma_commit(bar(BAR_ST_EMPTY + slot));
                     ++st_cnt;
+                    if (pv_next < jj) {
+                        const int r = issue_pv(pv_next, false);
+                        if (r < 0) {
+                            ok = false;
+                            break;
+                        }
+                        pv_next += r;
+                    }
                 }
                 if (!ok) break;
-                mma_commit(bar(BAR_S_FULL + sb));
-                if (jj >= 1 && !issue_pv(jj - 1)) {
+                // this half's latent columns last: the V chunks double as K
+                if (!mbar_wait(bar(BAR_V_FULL + sb), (jj >> 1) & 1, deadline, abort_flag)) {
                     ok = false;
                     break;
                 }
+                tc_fence_after();
+                for (int c = 0; c < kVChunks; ++c) {
+                    const uint32_t qa = sQ + (kVChunks * half + c) * kChunkBytesQ;
+                    const uint32_t kb = sV + sb * kVSetBytes + c * kChunkBytesKV;
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ss(dS, desc_sw128(qa + ks * 32, 16, 1024), desc_sw128(kb + ks * 32, 16, 1024), idS, 1u);
+                }
+                mma_commit(bar(BAR_S_FULL + sb));
+                while (ok && pv_next < jj) {
+                    if (issue_pv(pv_next, true) < 0) ok = false;
+                    else ++pv_next;
+                }
             }
-            if (ok) ok = issue_pv(nt - 1);
+            if (ok && issue_pv(nt - 1, true) < 0) ok = false;
             if (ok) {
                 mma_commit(bar(BAR_O_FINAL));
             } else {
@@ -402,13 +448,16 @@ __global__ void __launch_bounds__(192, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(BAR_S_FREE + sb));
             // scale, mask, tile max
+            uint64_t vis = ~0ull;
+            if (!node_ok) vis = 0;
+            else if (key0 + kKeys > T) vis = tile_visibility(key0, T, n, m0, m1);
+            const uint32_t vis_lo = static_cast<uint32_t>(vis), vis_hi = static_cast<uint32_t>(vis >> 32);
             float x[64];
             float mx = -INFINITY;
-            const bool all_prefix = key0 + kKeys <= T;
 #pragma unroll
             for (int k = 0; k < 64; ++k) {
-                const bool vis = node_ok && (all_prefix || key_visible(key0 + k, T, n, m0, m1));
-                x[k] = vis ? __uint_as_float(sv[k]) * a.scale_log2 : -INFINITY;
+                const uint32_t bit = (k < 32 ? (vis_lo >> k) : (vis_hi >> (k - 32))) & 1u;
+                x[k] = bit ? __uint_as_float(sv[k]) * a.scale_log2 : -INFINITY;
                 mx = fmaxf(mx, x[k]);
             }
             // P buffer sb was last read by PV of tile jj-2
@@ -443,16 +492,18 @@ __global__ void __launch_bounds__(192, 1)
                     tmem_wait_st();
                 }
             }
-            // probabilities (fp16) into tensor memory; the row sum adds the
-            // rounded values the PV product consumes
+            // probabilities (fp16) into tensor memory. While no key has been
+            // visible yet m_ref is -inf and every x is -inf: subtracting 0
+            // instead keeps p = 0 without a per-element test. The row sum
+            // adds the fp32 values (fp16 rounding is unbiased, 2^-11 each).
             uint32_t pk[32];
-            const bool live = m_ref != -INFINITY;
+            const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-                const float p0 = live ? ex2_approx(x[2 * k] - m_ref) : 0.f;
-                const float p1 = live ? ex2_approx(x[2 * k + 1] - m_ref) : 0.f;
+                const float p0 = ex2_approx(x[2 * k] - mref);
+                const float p1 = ex2_approx(x[2 * k + 1] - mref);
                 pk[k] = pack_f16x2(p0, p1);
-                l_sum += f16lo_to_f32(pk[k]) + f16hi_to_f32(pk[k]);
+                l_sum += p0 + p1;
             }
             tmem_st32(tmem + lane_base + kColP + sb * 32, pk);
             // S of this tile is complete, so its V chunks (read as bf16 K by
@@ -462,19 +513,24 @@ __global__ void __launch_bounds__(192, 1)
             {
                 uint4 *vset = reinterpret_cast<uint4 *>(smem + kOffV + sb * kVSetBytes);
                 const int kvalid = kend - key0;  // keys of this tile that exist
-#pragma unroll 4
-                for (int e = row; e < kVSetBytes / 16; e += kRows) {
-                    const int key = (e >> 3) & (kKeys - 1);  // 8 units of 16 B per 128-B key row
-                    uint4 v = vset[e];
-                    if (key < kvalid) {
-                        v.x = bf16x2_to_f16x2(v.x);
-                        v.y = bf16x2_to_f16x2(v.y);
-                        v.z = bf16x2_to_f16x2(v.z);
-                        v.w = bf16x2_to_f16x2(v.w);
-                    } else {
-                        v = make_uint4(0, 0, 0, 0);
+#pragma unroll 1
+                for (int e0 = row; e0 < kVSetBytes / 16; e0 += 4 * kRows) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) v[u] = vset[e0 + u * kRows];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int key = ((e0 + u * kRows) >> 3) & (kKeys - 1);  // 8 units of 16 B per key row
+                        if (key < kvalid) {
+                            v[u].x = bf16x2_to_f16x2(v[u].x);
+                            v[u].y = bf16x2_to_f16x2(v[u].y);
+                            v[u].z = bf16x2_to_f16x2(v[u].z);
+                            v[u].w = bf16x2_to_f16x2(v[u].w);
+                        } else {
+                            v[u] = make_uint4(0, 0, 0, 0);
+                        }
+                        vset[e0 + u * kRows] = v[u];
                     }
-                    vset[e] = v;
                 }
                 fence_proxy_async_smem();
             }
@@ -653,7 +709,7 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
         a.lse_dst = out.lse;
     }
     dim3 grid(plan.mtiles * 2, plan.nsplit, tree.B);
-    verify_attn_kernel<<<grid, 192, kSmemBytes, s>>>(tm_q, tm_kv, tm_kr, a);
+    verify_attn_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_q, tm_kv, tm_kr, a);
     if (cudaGetLastError() != cudaSuccess) return DDT_E_CUDA;
     if (plan.nsplit > 1) {
         merge_chunks_kernel<<<static_cast<unsigned>(rows_total), 128, 0, s>>>(
