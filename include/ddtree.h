@@ -64,7 +64,8 @@ enum {
     DDT_E_CUDA = 2,
     DDT_E_UNSUPPORTED = 3,
     DDT_E_BADINPUT = 4,
-    DDT_E_TIMEOUT = 5
+    DDT_E_TIMEOUT = 5,
+    DDT_E_SCRATCH_LIMIT = 6  /* ddt_verify_mla_attn_noalloc: shape needs more scratch than it holds */
 };
 
 #define DDT_MAX_DEPTH 16   /* D */
@@ -167,6 +168,36 @@ int ddt_verify_step(const ddt_draft *draft, int budget, ddt_tree *tree,
                     const ddt_attn_in *attn, float scale, ddt_attn_out *attn_out,
                     const int32_t *target_argmax, ddt_accept *acc, void *workspace,
                     size_t ws_bytes, void *stream);
+
+/* Bytes of device scratch held by ddt_verify_mla_attn_noalloc (64 MiB). */
+#define DDT_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* Step 2 for callers that cannot allocate device memory. The pages have no
+ * counterpart; this is a convenience of this library.
+ *
+ * ddt_verify_mla_attn needs a workspace from the caller whenever it splits
+ * each sequence's keys over several CTAs. Some callers cannot provide one:
+ * a serving engine that reserves nearly all HBM for its KV cache at start-up
+ * and has no allocator left to hand out more, a plugin or C host that is
+ * given only its input and output buffers, or code that must not call
+ * cudaMalloc because cudaMalloc synchronises the device. This call computes
+ * exactly what ddt_verify_mla_attn computes (same kernels, same arguments
+ * without the workspace) using a scratch array that the library defines at
+ * file scope: DDT_NOALLOC_SCRATCH_BYTES on every GPU that loads the library,
+ * held until the process exits. It allocates nothing.
+ *
+ *  - Shapes whose key-range partials would not fit return
+ *    DDT_E_SCRATCH_LIMIT before anything is enqueued (ddt_workspace_size
+ *    tells how much a shape needs on the current device).
+ *  - The first call on a device looks up the scratch array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Nothing in it needs to start at zero: a call writes every partial it
+ *    later reads. Calls whose kernels overlap on the GPU (several streams,
+ *    or several host threads) race on the array: serialise them. */
+int ddt_verify_mla_attn_noalloc(const ddt_attn_in *in, const ddt_tree *tree, float scale,
+                                ddt_attn_out *out, void *stream);
 
 /* Static text for a status code. */
 const char *ddt_status_str(int code);

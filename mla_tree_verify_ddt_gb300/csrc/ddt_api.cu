@@ -163,6 +163,7 @@ const char *ddt_status_str(int code) {
         case DDT_E_UNSUPPORTED: return "device is not sm_103";
         case DDT_E_BADINPUT: return "bad input data (drafter rows, token ids or prefix length)";
         case DDT_E_TIMEOUT: return "bounded on-chip wait expired";
+        case DDT_E_SCRATCH_LIMIT: return "shape needs more scratch than the no-allocation entry point holds";
         default: return "unknown status";
     }
 }

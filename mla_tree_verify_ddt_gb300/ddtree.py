@@ -17,11 +17,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libddtree.so")
 
 DDT_OK, DDT_E_INVAL, DDT_E_CUDA, DDT_E_UNSUPPORTED, DDT_E_BADINPUT, DDT_E_TIMEOUT = range(6)
+DDT_E_SCRATCH_LIMIT = 6
+NOALLOC_SCRATCH_BYTES = 64 << 20
 MAX_DEPTH, MAX_TOPK, MAX_BUDGET, LATENT, ROPE = 16, 16, 64, 512, 64
 
 EXPORTED = ["ddt_workspace_size", "ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept",
             "ddt_verify_step", "ddt_status_str", "ddt_read_device_status",
-            "ddt_selftest_bounded_wait"]
+            "ddt_selftest_bounded_wait", "ddt_verify_mla_attn_noalloc"]
 
 P = ctypes.c_void_p
 I = ctypes.c_int
@@ -78,12 +80,15 @@ def lib() -> ctypes.CDLL:
                                       ctypes.POINTER(DdtAttnIn), ctypes.c_float,
                                       ctypes.POINTER(DdtAttnOut), P, ctypes.POINTER(DdtAccept), P,
                                       ctypes.c_size_t, P]
+        L.ddt_verify_mla_attn_noalloc.argtypes = [ctypes.POINTER(DdtAttnIn), ctypes.POINTER(DdtTree),
+                                                  ctypes.c_float, ctypes.POINTER(DdtAttnOut), P]
         L.ddt_status_str.argtypes = [I]
         L.ddt_status_str.restype = ctypes.c_char_p
         L.ddt_read_device_status.argtypes = [P, I, P]
         L.ddt_selftest_bounded_wait.argtypes = [P, ctypes.c_uint, P]
         for f in ("ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept", "ddt_verify_step",
-                  "ddt_read_device_status", "ddt_selftest_bounded_wait"):
+                  "ddt_read_device_status", "ddt_selftest_bounded_wait",
+                  "ddt_verify_mla_attn_noalloc"):
             getattr(L, f).restype = I
         _lib = L
     return _lib
@@ -214,6 +219,27 @@ def ddt_verify_mla_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: Tree, sca
     _check(lib().ddt_verify_mla_attn(ctypes.byref(a), ctypes.byref(t), float(scale),
                                      ctypes.byref(o), _ptr(workspace), wsb, _stream_ptr(stream)),
            "ddt_verify_mla_attn")
+    return out, lse
+
+
+def ddt_verify_mla_attn_noalloc(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: Tree, scale: float,
+                                out=None, lse=None, stream=None):
+    """Same as ddt_verify_mla_attn, for callers that cannot allocate: the
+    key-range partials go to the library's own fixed device scratch
+    (NOALLOC_SCRATCH_BYTES per GPU). Output tensors, if not given, are
+    created here by torch; pass them in to allocate nothing at all."""
+    _contig(q_lat, q_rope, c_kv, k_rope, prefix_len)
+    B, Qc, H, _ = q_lat.shape
+    if out is None:
+        out = torch.empty(B, Qc, H, LATENT, dtype=torch.float32, device=q_lat.device)
+    if lse is None:
+        lse = torch.empty(B, Qc, H, dtype=torch.float32, device=q_lat.device)
+    a = attn_in_struct(q_lat, q_rope, c_kv, k_rope, prefix_len)
+    o = DdtAttnOut(_ptr(out), _ptr(lse))
+    t = tree.c()
+    _check(lib().ddt_verify_mla_attn_noalloc(ctypes.byref(a), ctypes.byref(t), float(scale),
+                                             ctypes.byref(o), _stream_ptr(stream)),
+           "ddt_verify_mla_attn_noalloc")
     return out, lse
 
 
