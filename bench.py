@@ -48,6 +48,18 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value over all replica ranks (host-side gloo collective; the
+    timed path has no data exchange between GPUs)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -325,11 +337,7 @@ def gpu_arm(args, wl_idx, rank, world, local_rank):
     if pg:
         pg.barrier()
     step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-    total_ms = sum(step_ms)
-    if pg:
-        t = torch.tensor([total_ms])
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
     value = world * 1000.0 / ms_per_step
 

@@ -14,37 +14,44 @@
 // Message", section "Architectural Abstraction" (nodes at positions L+depth,
 // mask [ones | visibility]).
 //
-// Design (one CTA = 128 query rows x one half of the 512 output columns x one
-// range of keys):
-//  * rows are (node, head) pairs of one sequence, so every row of a tile
-//    shares the sequence's KV: one 64-key KV tile feeds all 128 rows;
-//  * S = Q K^T (M=128, N=64, K=576) and O += P V (M=128, N=256, K=64) run on
-//    tcgen05 with fp32 accumulators in tensor memory. O for 128 rows x 512
-//    columns would fill all 512 TMEM columns, leaving none for S, so each
-//    CTA owns one 256-column half of O and recomputes S (the partner CTA of
-//    the other half computes the same S bit for bit);
-//  * the 512 latent query columns stay resident in shared memory (TMA,
-//    128-byte swizzle); the 64 rotary query columns and the probabilities P
-//    live in tensor memory and feed the MMA as its A operand;
-//  * KV arrives by TMA in 64-column chunks: the four chunks that are this
-//    half's V are double-buffered per tile and serve both S and PV; the other
-//    five chunks stream through a 4-slot ring fed by a second producer warp,
-//    so ring loads never queue behind V loads. S consumes the streamed chunks
-//    first and the V chunks last, and a ready PV is slipped in between S
-//    chunks;
-//  * softmax runs on 4 warps, one thread per row, in fp32 in the log2 domain,
-//    with a lazily moved reference max (O is rescaled only when a row's max
-//    grows by more than 2^8);
-//  * PV runs in fp16 (P rounded to fp16, 2^-11 relative, four times tighter
-//    than bf16): after S of a tile has read its V chunks as bf16 K, the
-//    softmax warps convert those chunks to fp16 in place;
-//  * the softmax code is kept compact (visibility as one 64-bit word per
-//    tile, rolled loops off the per-key path): the fully unrolled version
-//    spent most of its time waiting for instruction fetch;
-//  * when the key range is split over several CTAs, each writes a normalised
-//    partial and its lse; a second kernel merges them.
-// Every mbarrier wait is bounded; on expiry the CTA records DDT_E_TIMEOUT in
-// the sequence's status word and leaves after draining its own copies.
+// Design. A cluster of two CTAs (ranks r = 0, 1) owns 128 (node, head) rows
+// of one sequence and one range of its keys. All rows share the sequence's
+// KV, so one 64-key KV tile feeds 128 rows.
+//  * Split along the 576-wide contraction: CTA r holds the query columns of
+//    latent dims [256r, 256r+256) and rotary dims [32r, 32r+32), loads the
+//    same columns of every KV tile, and computes a partial S (M=128 rows,
+//    N=64 keys, K=288) into tensor memory. Its 256 latent KV columns are also
+//    the V of its half of the output, so O += P V (M=128, N=256, K=64) needs
+//    no further load. Nothing is computed twice and each CTA keeps only part
+//    of Q and half of each KV row (36 KB per 64-key tile) in shared memory,
+//    which leaves room for four KV tiles in flight.
+//  * Tensor memory: O (256 columns), three S buffers of 64 columns, and the
+//    query's fourth latent chunk plus its rotary part as MMA A operands (the
+//    other three latent chunks are in shared memory). Each thread overwrites
+//    its own lane of S with the P of that tile once it has read S, so S and
+//    P share buffers and a buffer is reused three tiles later, after its PV.
+//  * Rows [64r, 64r+64) are "owned" by CTA r. For each tile the two warps of
+//    the other rows ship their partial-S rows to the partner through
+//    distributed shared memory; the owner warps add the partner's partial to
+//    their own, run the softmax, and ship the probabilities back. Shipping
+//    uses st.async, whose bytes are credited to the receiver's mbarrier on
+//    arrival: a remote store followed by a release-arrive made the sender
+//    wait for the round trip (about 0.8 us). Every row
+//    ends up with P in both CTAs' tensor memory, each CTA multiplies by its
+//    own V half.
+//  * Softmax in fp32, log2 domain, one thread per row, visibility as one
+//    64-bit word per tile (all ones inside the prefix). The reference max
+//    moves lazily: O is rescaled only when a row's max grows by more than 8
+//    (log2 units), so probabilities stay <= 256; the factor travels with P.
+//  * P goes to the tensor core as two bf16 terms, hi = bf16(p) and
+//    lo = bf16(p - hi), each an A operand from tensor memory against the same
+//    bf16 V; together they carry p to about 2^-17 relative.
+//  * KV rows past the last node may hold anything; the tail tile's V rows
+//    there are zeroed in shared memory before the PV product reads them.
+//  * When the key range is split over several clusters, each writes a
+//    normalised partial and its lse; a second kernel merges them.
+// Every on-chip wait is bounded; on expiry the CTA records DDT_E_TIMEOUT in
+// the sequence's status word, drains its own copies and MMAs and leaves.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -58,49 +65,59 @@
 namespace ddt {
 namespace {
 
-constexpr int kRows = 128;        // query rows per CTA (MMA M)
-constexpr int kKeys = 64;         // keys per tile (S MMA N)
-constexpr int kChunkBytesQ = kRows * 128;   // 64 bf16 columns x 128 rows
-constexpr int kChunkBytesKV = kKeys * 128;  // 64 bf16 columns x 64 keys
-constexpr int kQChunks = 8;       // latent query: 512 columns
-constexpr int kVChunks = 4;       // this CTA's half of the latent (256 columns)
-constexpr int kStreamSlots = 4;
-constexpr int kStreamPerTile = 5; // the other latent half (4) + rotary key (1)
+constexpr int kRows = 128;          // rows per cluster (MMA M)
+constexpr int kOwnRows = 64;        // rows whose softmax one CTA runs
+constexpr int kKeys = 64;           // keys per tile (S MMA N)
+constexpr int kQChunks = 4;         // latent query/KV chunks per CTA: 4 x 64 columns
+constexpr int kQSmemChunks = 3;     // query chunks 0-2 in shared memory; chunk 3 and the
+                                    // rotary columns sit in tensor memory (A operands)
+constexpr int kChunkBytesQ = kRows * 128;    // 64 bf16 x 128 rows, 128-byte swizzle
+constexpr int kChunkBytesKV = kKeys * 128;   // 64 bf16 x 64 keys
+constexpr int kKRopeBytes = kKeys * 64;      // 32 bf16 x 64 keys, 64-byte swizzle
+constexpr int kSlotBytes = kQChunks * kChunkBytesKV + kKRopeBytes;  // 36864
+constexpr int kSlots = 4;           // KV tiles in flight
+constexpr int kSPBufs = 3;          // S / P buffers in tensor memory
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffQ = 0;
-constexpr int kOffV = kOffQ + kQChunks * kChunkBytesQ;            // 131072
-constexpr int kVSetBytes = kVChunks * kChunkBytesKV;              // 32768
-constexpr int kOffStream = kOffV + 2 * kVSetBytes;                // 196608
-constexpr int kOffBar = kOffStream + kStreamSlots * kChunkBytesKV; // 229376
+constexpr int kOffRing = kOffQ + kQSmemChunks * kChunkBytesQ;     // 49152
+constexpr int kOffSX = kOffRing + kSlots * kSlotBytes;            // 196608: partner's partial S, my rows
+constexpr int kSXBytes = kOwnRows * kKeys * 4;                    // 16384
+constexpr int kOffPX = kOffSX + kSXBytes;                         // 212992: partner's P (hi, lo) for my other rows
+constexpr int kPXBytes = kOwnRows * kKeys * 4;                    // 16384 (32 hi + 32 lo words per row)
+constexpr int kOffAX = kOffPX + kPXBytes;                         // 229376: rescale factor per row
+constexpr int kOffLX = kOffAX + kOwnRows * 4;                     // 229632: final row sum per row
+constexpr int kOffBar = kOffLX + kOwnRows * 4;                    // 229888
 constexpr int kSmemBytes = kOffBar + 256 + 1024;                  // + alignment slack
 
 // tensor memory columns
-constexpr uint32_t kColO = 0;     // 256 columns: this CTA's half of O
-constexpr uint32_t kColS = 256;   // 2 x 64: S double buffer
-constexpr uint32_t kColP = 384;   // 2 x 32: P (fp16 pairs) double buffer
-constexpr uint32_t kColQR = 448;  // 32: rotary query (bf16 pairs)
+constexpr uint32_t kColO = 0;       // 256: this CTA's half of O
+constexpr uint32_t kColSP = 256;    // 3 x 64: partial S of a tile, overwritten in place (lane by
+                                    // lane, once read) by its P: 32 hi words then 32 lo words
+constexpr uint32_t kColQ3 = 448;    // 32: latent query chunk 3 (bf16 pairs)
+constexpr uint32_t kColQR = 480;    // 16: rotary query (bf16 pairs)
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// warps 0-3 softmax/epilogue, 4 TMA (Q, V), 5 MMA, 6 TMA (streamed chunks)
-constexpr int kThreads = 224;
+constexpr int kThreads = 192;  // warps 0-3 softmax group, 4 TMA producer, 5 MMA issuer
 
-// barrier indices
 enum {
     BAR_Q_FULL = 0,
-    BAR_V_FULL = 1,      // 2
-    BAR_V_EMPTY = 3,     // 2
-    BAR_ST_FULL = 5,     // 4
-    BAR_ST_EMPTY = 9,    // 4
-    BAR_QR_READY = 13,
-    BAR_S_FULL = 14,     // 2
-    BAR_S_FREE = 16,     // 2
-    BAR_P_FULL = 18,     // 2
-    BAR_PV_DONE = 20,    // 2
-    BAR_O_FINAL = 22,
-    BAR_DRAIN = 23,
-    NUM_BARS = 24
+    BAR_QT_READY = 1,    // query chunk 3 and rotary query written to tensor memory
+    BAR_RING_FULL = 2,   // kSlots
+    BAR_RING_EMPTY = 6,  // kSlots
+    BAR_S_FULL = 10,     // kSPBufs
+    BAR_P_FULL = 13,     // kSPBufs
+    BAR_PV_DONE = 16,    // kSPBufs
+    BAR_O_FINAL = 19,
+    BAR_DRAIN = 20,
+    // exchange barriers, arrived on by the partner CTA's threads
+    BAR_SX_FULL = 21,    // partner wrote its partial S rows into my SX
+    BAR_SX_EMPTY = 22,   // partner read the partial S rows I wrote into its SX
+    BAR_PX_FULL = 23,    // partner wrote P for my other rows into my PX
+    BAR_PX_EMPTY = 24,   // partner read the P I wrote into its PX
+    BAR_LX_FULL = 25,    // partner wrote final row sums into my LX
+    NUM_BARS = 26
 };
 
 struct AttnArgs {
@@ -108,6 +125,7 @@ struct AttnArgs {
     const uint64_t *mask;
     const int32_t *n_nodes;
     const int32_t *prefix_len;
+    const uint16_t *q_lat;   // for query chunk 3, loaded straight into tensor memory
     const uint16_t *q_rope;
     int32_t *status;
     float *o_dst;            // [nsplit][rows_total][512] (nsplit == 1: the final output)
@@ -120,7 +138,8 @@ struct AttnArgs {
 // Visibility of keys key0..key0+63 for a node with ancestor mask (m0, m1):
 // every prefix key (< T) and the keys T+m of ancestors-or-self m < n. Only
 // tiles that reach past the prefix need it; the loop stays rolled to keep
-// the softmax code small.
+// the softmax code small (a fully unrolled per-key test made the softmax
+// warps wait on instruction fetch).
 __device__ __noinline__ uint64_t tile_visibility(int key0, int T, int n, uint64_t m0, uint64_t m1) {
     uint64_t vis = 0;
 #pragma unroll 1
@@ -138,19 +157,19 @@ __device__ __noinline__ uint64_t tile_visibility(int key0, int T, int n, uint64_
     return vis;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    verify_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_kv,
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    verify_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                        const __grid_constant__ CUtensorMap tm_kr, const AttnArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.x >> 1;
-    const int half = blockIdx.x & 1;
+    const uint32_t rank = cluster_ctarank();  // == blockIdx.x & 1
+    const uint32_t peer = rank ^ 1u;
     const int chunk = blockIdx.y;
     const int b = blockIdx.z;
 
-    // ---- per-sequence key range (uniform over the CTA)
+    // ---- per-sequence key range (uniform over the cluster)
     const int T = a.prefix_len[b];
     int n = a.n_nodes[b];
     n = n < 1 ? 1 : (n > a.Qc ? a.Qc : n);
@@ -165,25 +184,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *o_dst = a.o_dst + static_cast<size_t>(chunk) * a.rows_total * 512;
     float *lse_dst = a.lse_dst + static_cast<size_t>(chunk) * a.rows_total;
 
-    if (!seq_ok && tid == 0 && mt == 0 && half == 0 && chunk == 0) a.status[b] = DDT_E_BADINPUT;
+    if (!seq_ok && tid == 0 && mt == 0 && rank == 0 && chunk == 0) a.status[b] = DDT_E_BADINPUT;
 
     if (nt <= 0) {
-        // nothing visible in this range: zero rows, lse = -inf
-        for (int idx = tid; idx < kRows * 64; idx += blockDim.x) {
+        // nothing visible in this range: zero rows (this CTA's half), lse = -inf
+        for (int idx = tid; idx < kRows * 64; idx += kThreads) {
             const int r = idx >> 6, c4 = idx & 63;
             const int g = mt * kRows + r;
             if (g >= rows_seq) continue;
-            float4 *dst = reinterpret_cast<float4 *>(o_dst + (row_base + g) * 512 + half * 256) + c4;
+            float4 *dst = reinterpret_cast<float4 *>(o_dst + (row_base + g) * 512 + rank * 256) + c4;
             *dst = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (half == 0 && c4 == 0) lse_dst[row_base + g] = -INFINITY;
+            if (rank == 0 && c4 == 0) lse_dst[row_base + g] = -INFINITY;
         }
-        return;
+        return;  // both CTAs of the cluster leave here together
     }
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + kOffQ, sV = sbase + kOffV, sST = sbase + kOffStream;
+    const uint32_t sQ = sbase + kOffQ, sRing = sbase + kOffRing;
     const uint32_t sBar = sbase + kOffBar;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + NUM_BARS * 8 + 4);
@@ -191,21 +210,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(bar(BAR_Q_FULL), 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(BAR_V_FULL + s), 1);
-            mbar_init(bar(BAR_V_EMPTY + s), 1);
+        mbar_init(bar(BAR_QT_READY), 4);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(bar(BAR_RING_FULL + s), 1);
+            mbar_init(bar(BAR_RING_EMPTY + s), 1);
+        }
+        for (int s = 0; s < kSPBufs; ++s) {
             mbar_init(bar(BAR_S_FULL + s), 1);
-            mbar_init(bar(BAR_S_FREE + s), 4);
             mbar_init(bar(BAR_P_FULL + s), 4);
             mbar_init(bar(BAR_PV_DONE + s), 1);
         }
-        for (int s = 0; s < kStreamSlots; ++s) {
-            mbar_init(bar(BAR_ST_FULL + s), 1);
-            mbar_init(bar(BAR_ST_EMPTY + s), 1);
-        }
-        mbar_init(bar(BAR_QR_READY), 4);
         mbar_init(bar(BAR_O_FINAL), 1);
         mbar_init(bar(BAR_DRAIN), 1);
+        // the FULL barriers complete on bytes: one local thread arms each
+        // phase with expect_tx and the partner's st.async credits the bytes
+        mbar_init(bar(BAR_SX_FULL), 1);
+        mbar_init(bar(BAR_SX_EMPTY), kOwnRows);
+        mbar_init(bar(BAR_PX_FULL), 1);
+        mbar_init(bar(BAR_PX_EMPTY), kOwnRows);
+        mbar_init(bar(BAR_LX_FULL), 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -214,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    // both CTAs' barriers must exist before either sends the other anything
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint64_t deadline = globaltimer_ns() + a.wait_ns;
@@ -225,28 +249,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (warp == 4) {
-        // ================= TMA producer: Q once, then this half's V chunks =================
+        // ======================= TMA producer =======================
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_kv);
+            tma_prefetch_desc(&tm_kr);
             const int qrow = static_cast<int>(row_base) + mt * kRows;
-            mbar_arrive_expect_tx(bar(BAR_Q_FULL), kQChunks * kChunkBytesQ);
-            for (int c = 0; c < kQChunks; ++c)
-                tma_load_2d(sQ + c * kChunkBytesQ, &tm_q, c * 64, qrow, bar(BAR_Q_FULL));
-            int armed_v[2] = {0, 0};
+            mbar_arrive_expect_tx(bar(BAR_Q_FULL), kQSmemChunks * kChunkBytesQ);
+            for (int c = 0; c < kQSmemChunks; ++c)
+                tma_load_2d(sQ + c * kChunkBytesQ, &tm_q, static_cast<int>(rank) * 256 + c * 64, qrow,
+                            bar(BAR_Q_FULL));
+            int armed[kSlots] = {0, 0, 0, 0};
             bool ok = true;
             for (int jj = 0; jj < nt; ++jj) {
-                const int key_row = b * a.Tcap + (t0 + jj) * kKeys;
-                const int vs = jj & 1;
-                if (jj >= 2 && !mbar_wait(bar(BAR_V_EMPTY + vs), ((jj - 2) >> 1) & 1, deadline, abort_flag)) {
+                const int slot = jj % kSlots, use = jj / kSlots;
+                if (use >= 1 && !mbar_wait(bar(BAR_RING_EMPTY + slot), (use - 1) & 1, deadline, abort_flag)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bar(BAR_V_FULL + vs), kVSetBytes);
-                ++armed_v[vs];
-                for (int c = 0; c < kVChunks; ++c)
-                    tma_load_2d(sV + vs * kVSetBytes + c * kChunkBytesKV, &tm_kv,
-                                (kVChunks * half + c) * 64, key_row, bar(BAR_V_FULL + vs));
+                const int key_row = b * a.Tcap + (t0 + jj) * kKeys;
+                const uint32_t dst = sRing + slot * kSlotBytes;
+                mbar_arrive_expect_tx(bar(BAR_RING_FULL + slot), kSlotBytes);
+                ++armed[slot];
+                for (int c = 0; c < kQChunks; ++c)
+                    tma_load_2d(dst + c * kChunkBytesKV, &tm_kv, static_cast<int>(rank) * 256 + c * 64, key_row,
+                                bar(BAR_RING_FULL + slot));
+                tma_load_2d(dst + kQChunks * kChunkBytesKV, &tm_kr, static_cast<int>(rank) * 32, key_row,
+                            bar(BAR_RING_FULL + slot));
             }
             if (!ok) {
                 fail();
@@ -254,130 +283,93 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t drain_deadline = globaltimer_ns() + 100000000ull;
                 const int zero = 0;
                 mbar_wait(bar(BAR_Q_FULL), 0, drain_deadline, &zero);
-                for (int s = 0; s < 2; ++s)
-                    if (armed_v[s]) mbar_wait(bar(BAR_V_FULL + s), (armed_v[s] - 1) & 1, drain_deadline, &zero);
-            }
-        }
-    } else if (warp == 6) {
-        // ====== TMA producer: the other latent half and the rotary key, through the ring ======
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_kr);
-            int armed_st[kStreamSlots] = {0, 0, 0, 0};
-            int st_cnt = 0;
-            bool ok = true;
-            for (int jj = 0; jj < nt && ok; ++jj) {
-                const int key_row = b * a.Tcap + (t0 + jj) * kKeys;
-                for (int q = 0; q < kStreamPerTile; ++q) {
-                    const int slot = st_cnt % kStreamSlots, use = st_cnt / kStreamSlots;
-                    if (use >= 1 && !mbar_wait(bar(BAR_ST_EMPTY + slot), (use - 1) & 1, deadline, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar(BAR_ST_FULL + slot), kChunkBytesKV);
-                    ++armed_st[slot];
-                    if (q < 4)
-                        tma_load_2d(sST + slot * kChunkBytesKV, &tm_kv,
-                                    (kVChunks * (1 - half) + q) * 64, key_row, bar(BAR_ST_FULL + slot));
-                    else
-                        tma_load_2d(sST + slot * kChunkBytesKV, &tm_kr, 0, key_row,
-                                    bar(BAR_ST_FULL + slot));
-                    ++st_cnt;
-                }
-            }
-            if (!ok) {
-                fail();
-                const uint64_t drain_deadline = globaltimer_ns() + 100000000ull;
-                const int zero = 0;
-                for (int s = 0; s < kStreamSlots; ++s)
-                    if (armed_st[s]) mbar_wait(bar(BAR_ST_FULL + s), (armed_st[s] - 1) & 1, drain_deadline, &zero);
+                for (int s = 0; s < kSlots; ++s)
+                    if (armed[s]) mbar_wait(bar(BAR_RING_FULL + s), (armed[s] - 1) & 1, drain_deadline, &zero);
             }
         }
     } else if (warp == 5) {
         // ======================= MMA issuer =======================
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_f32acc(kRows, kKeys, 1, 0, 0);   // bf16 Q, K
-            constexpr uint32_t idPV = idesc_f32acc(kRows, 256, 0, 0, 1);  // fp16 P, V (MN-major)
+            constexpr uint32_t idS = idesc_f32acc(kRows, kKeys, 1, 0, 0);   // bf16 Q, K (K-major)
+            constexpr uint32_t idPV = idesc_f32acc(kRows, 256, 1, 0, 1);  // bf16 P (TMEM), V (MN-major)
             bool ok = mbar_wait(bar(BAR_Q_FULL), 0, deadline, abort_flag) &&
-                      mbar_wait(bar(BAR_QR_READY), 0, deadline, abort_flag);
+                      mbar_wait(bar(BAR_QT_READY), 0, deadline, abort_flag);
             tc_fence_after();
-            int st_cnt = 0;
             int pv_next = 0;  // the next tile whose PV is still to be issued
-            // O += P_j V_j once the softmax has published P_j. With block ==
-            // false it only issues when P_j is already there, so a PV can slip
-            // in between the chunks of the next S as soon as it is ready.
+            // O += P_j V_j (both bf16 terms of P) once P_j is in tensor memory.
+            // With block == false it only issues when P_j is already there.
             auto issue_pv = [&](int j, bool block) -> int {
-                const int pb = j & 1;
+                const int pb = j % kSPBufs;
                 if (block) {
-                    if (!mbar_wait(bar(BAR_P_FULL + pb), (j >> 1) & 1, deadline, abort_flag)) return -1;
-                } else if (!mbar_try_wait(bar(BAR_P_FULL + pb), (j >> 1) & 1)) {
+                    if (!mbar_wait(bar(BAR_P_FULL + pb), (j / kSPBufs) & 1, deadline, abort_flag)) return -1;
+                } else if (!mbar_try_wait(bar(BAR_P_FULL + pb), (j / kSPBufs) & 1)) {
                     return 0;
                 }
                 tc_fence_after();
-                const uint32_t vb = sV + pb * kVSetBytes;
+                const int slot = j % kSlots;
+                const uint32_t vb = sRing + slot * kSlotBytes;
+                const uint32_t pcol = tmem + kColSP + pb * 64;
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    mma_ts(tmem + kColO, tmem + kColP + pb * 32 + ks * 8,
-                           desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV,
+                    mma_ts(tmem + kColO, pcol + ks * 8, desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV,
                            (j > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < kKeys / 16; ++ks)
+                    mma_ts(tmem + kColO, pcol + 32 + ks * 8, desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV,
+                           1u);
                 mma_commit(bar(BAR_PV_DONE + pb));
-                mma_commit(bar(BAR_V_EMPTY + pb));
+                mma_commit(bar(BAR_RING_EMPTY + slot));
                 return 1;
             };
+            auto try_pv = [&]() -> bool {
+                if (pv_next >= nt) return true;
+                const int r = issue_pv(pv_next, false);
+                if (r < 0) return false;
+                pv_next += r;
+                return true;
+            };
             for (int jj = 0; jj < nt && ok; ++jj) {
-                const int sb = jj & 1;
-                if (jj >= 2 && !mbar_wait(bar(BAR_S_FREE + sb), ((jj - 2) >> 1) & 1, deadline, abort_flag)) {
+                const int sb = jj % kSPBufs, slot = jj % kSlots;
+                // a PV that became ready goes first
+                if (pv_next < jj && !try_pv()) {
                     ok = false;
                     break;
                 }
-                const uint32_t dS = tmem + kColS + sb * kKeys;
-                // the streamed chunks first: the other latent half and the rotary part
-                for (int q = 0; q < kStreamPerTile; ++q) {
-                    const int slot = st_cnt % kStreamSlots, use = st_cnt / kStreamSlots;
-                    if (!mbar_wait(bar(BAR_ST_FULL + slot), use & 1, deadline, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t kb = sST + slot * kChunkBytesKV;
-                    if (q < 4) {
-                        const uint32_t qa = sQ + (kVChunks * (1 - half) + q) * kChunkBytesQ;
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(dS, desc_sw128(qa + ks * 32, 16, 1024), desc_sw128(kb + ks * 32, 16, 1024),
-                                   idS, (q > 0 || ks > 0) ? 1u : 0u);
-                    } else {
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_ts(dS, tmem + kColQR + ks * 8, desc_sw128(kb + ks * 32, 16, 1024), idS, 1u);
-                    }
-                    mma_commit(bar(BAR_ST_EMPTY + slot));
-                    ++st_cnt;
-                    if (pv_next < jj) {
-                        const int r = issue_pv(pv_next, false);
-                        if (r < 0) {
-                            ok = false;
-                            break;
-                        }
-                        pv_next += r;
-                    }
+                // the S/P buffer of tile jj-3 is free once its PV is done
+                if (jj >= kSPBufs &&
+                    !mbar_wait(bar(BAR_PV_DONE + sb), ((jj - kSPBufs) / kSPBufs) & 1, deadline, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
-                // this half's latent columns last: the V chunks double as K
-                if (!mbar_wait(bar(BAR_V_FULL + sb), (jj >> 1) & 1, deadline, abort_flag)) {
+                if (!mbar_wait(bar(BAR_RING_FULL + slot), (jj / kSlots) & 1, deadline, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (int c = 0; c < kVChunks; ++c) {
-                    const uint32_t qa = sQ + (kVChunks * half + c) * kChunkBytesQ;
-                    const uint32_t kb = sV + sb * kVSetBytes + c * kChunkBytesKV;
+                const uint32_t dS = tmem + kColSP + sb * 64;
+                const uint32_t kb = sRing + slot * kSlotBytes;
+                for (int c = 0; c < kQSmemChunks; ++c)
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ss(dS, desc_sw128(qa + ks * 32, 16, 1024), desc_sw128(kb + ks * 32, 16, 1024), idS, 1u);
-                }
+                        mma_ss(dS, desc_sw128(sQ + c * kChunkBytesQ + ks * 32, 16, 1024),
+                               desc_sw128(kb + c * kChunkBytesKV + ks * 32, 16, 1024), idS,
+                               (c > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_ts(dS, tmem + kColQ3 + ks * 8, desc_sw128(kb + 3 * kChunkBytesKV + ks * 32, 16, 1024), idS,
+                           1u);
+                for (int ks = 0; ks < 2; ++ks)
+                    mma_ts(dS, tmem + kColQR + ks * 8, desc_sw64(kb + kQChunks * kChunkBytesKV + ks * 32, 512), idS,
+                           1u);
                 mma_commit(bar(BAR_S_FULL + sb));
-                while (ok && pv_next < jj) {
+                // P of a tile arrives after the next tile's S has gone round
+                // the cluster, so PV may trail S by up to two tiles; only
+                // then does the issuer wait for it
+                while (ok && pv_next < jj - 1) {
                     if (issue_pv(pv_next, true) < 0) ok = false;
                     else ++pv_next;
                 }
             }
-            if (ok && issue_pv(nt - 1, true) < 0) ok = false;
+            while (ok && pv_next < nt) {
+                if (issue_pv(pv_next, true) < 0) ok = false;
+                else ++pv_next;
+            }
             if (ok) {
                 mma_commit(bar(BAR_O_FINAL));
             } else {
@@ -389,164 +381,274 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ======================= softmax / epilogue (warps 0-3) =======================
-        const int row = warp * 32 + lane;
-        const int g = mt * kRows + row;           // row within the sequence
+        // ======================= softmax group (warps 0-3) =======================
+        const int row = warp * 32 + lane;            // TMEM lane of this thread
+        const bool owner = (row >> 6) == static_cast<int>(rank);
+        const int lr = row & (kOwnRows - 1);         // row index within its 64-row half
+        const int g = mt * kRows + row;              // row within the sequence
         const bool row_in_seq = g < rows_seq;
         const int node = g / a.H;
         const bool node_ok = row_in_seq && node < n && seq_ok;
         uint64_t m0 = 0, m1 = 0;
-        if (node_ok) {
+        if (owner && node_ok) {
             const uint64_t *mk = a.mask + (static_cast<size_t>(b) * a.Qc + node) * a.W;
             m0 = mk[0];
             if (a.W > 1) m1 = mk[1];
         }
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        // rotary query row -> tensor memory (bf16 pairs, low half = even column)
+        const uint4 *sx = reinterpret_cast<const uint4 *>(smem + kOffSX);   // [16][64 rows] of 4 floats
+        const uint4 *px = reinterpret_cast<const uint4 *>(smem + kOffPX);   // [16][64 rows] of 4 words
+        const volatile float *ax = reinterpret_cast<const volatile float *>(smem + kOffAX);
+        const volatile float *lx = reinterpret_cast<const volatile float *>(smem + kOffLX);
+        // the partner's copies of the exchange buffers and barriers
+        const uint32_t r_sx = mapa_shared(sbase + kOffSX, peer);
+        const uint32_t r_px = mapa_shared(sbase + kOffPX, peer);
+        const uint32_t r_ax = mapa_shared(sbase + kOffAX, peer);
+        const uint32_t r_lx = mapa_shared(sbase + kOffLX, peer);
+        const uint32_t r_bar_sx_full = mapa_shared(bar(BAR_SX_FULL), peer);
+        const uint32_t r_bar_sx_empty = mapa_shared(bar(BAR_SX_EMPTY), peer);
+        const uint32_t r_bar_px_full = mapa_shared(bar(BAR_PX_FULL), peer);
+        const uint32_t r_bar_px_empty = mapa_shared(bar(BAR_PX_EMPTY), peer);
+        const uint32_t r_bar_lx_full = mapa_shared(bar(BAR_LX_FULL), peer);
+
+        // waits of the softmax group are made warp-uniform, so a lane that
+        // gives up can never leave its warp split before a .sync.aligned op
+        auto wwait = [&](uint32_t barrier, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(barrier, parity, deadline, abort_flag));
+        };
+        auto wwait_cluster = [&](uint32_t barrier, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait_cluster(barrier, parity, deadline, abort_flag));
+        };
+
+        // this row's latent query chunk 3 and rotary query -> tensor memory,
+        // as bf16 pairs (low half = even column)
         {
-            uint32_t qr[32];
+            uint32_t q3[32], qr[32];
+#pragma unroll
+            for (int v = 0; v < 32; ++v) q3[v] = qr[v] = 0;
             if (row_in_seq) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(a.q_rope + (row_base + g) * 64);
+                const uint4 *s3 = reinterpret_cast<const uint4 *>(a.q_lat + (row_base + g) * 512 + rank * 256 + 192);
+                const uint4 *sr = reinterpret_cast<const uint4 *>(a.q_rope + (row_base + g) * 64 + rank * 32);
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
-                    const uint4 x = src[v];
-                    qr[4 * v + 0] = x.x;
+                    const uint4 x = s3[v];
+                    q3[4 * v] = x.x;
+                    q3[4 * v + 1] = x.y;
+                    q3[4 * v + 2] = x.z;
+                    q3[4 * v + 3] = x.w;
+                }
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const uint4 x = sr[v];
+                    qr[4 * v] = x.x;
                     qr[4 * v + 1] = x.y;
                     qr[4 * v + 2] = x.z;
                     qr[4 * v + 3] = x.w;
                 }
-            } else {
-#pragma unroll
-                for (int v = 0; v < 32; ++v) qr[v] = 0;
             }
-            tmem_st32(tmem + lane_base + kColQR, qr);
+            tmem_st32(tmem + lane_base + kColQ3, q3);
+            tmem_st16(tmem + lane_base + kColQR, *reinterpret_cast<const uint32_t(*)[16]>(&qr[0]));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_QR_READY));
+            if (lane == 0) mbar_arrive(bar(BAR_QT_READY));
         }
-        float m_ref = -INFINITY, l_sum = 0.f;
-        bool ok = true;
-        for (int jj = 0; jj < nt; ++jj) {
-            const int sb = jj & 1;
-            const int key0 = (t0 + jj) * kKeys;
-            if (!mbar_wait(bar(BAR_S_FULL + sb), (jj >> 1) & 1, deadline, abort_flag)) {
-                ok = false;
-                break;
-            }
+
+        // this thread's row of the partial S of tile t, from tensor memory
+        auto load_s = [&](int t, uint32_t (&sv)[64]) -> bool {
+            const int sb = t % kSPBufs;
+            if (!wwait(bar(BAR_S_FULL + sb), (t / kSPBufs) & 1)) return false;
             __syncwarp();
             tc_fence_after();
-            uint32_t sv[64];
-            {
-                uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-                uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-                tmem_ld32(tmem + lane_base + kColS + sb * kKeys, lo);
-                tmem_ld32(tmem + lane_base + kColS + sb * kKeys + 32, hi);
-                tmem_wait_ld();
+            uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+            uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+            tmem_ld32(tmem + lane_base + kColSP + sb * 64, lo);
+            tmem_ld32(tmem + lane_base + kColSP + sb * 64 + 32, hi);
+            tmem_wait_ld();
+            return true;
+        };
+        // P of tile t for this row into this CTA's tensor memory, over the
+        // row's own (already read) S of that tile, after the row's O has been
+        // rescaled by alpha; the rescale needs O quiescent (PV of t-1 done)
+        auto publish = [&](int t, float alpha, const uint32_t (&pk_hi)[32], const uint32_t (&pk_lo)[32]) -> bool {
+            const int pb = t % kSPBufs;
+            if (__any_sync(0xffffffffu, alpha != 1.0f) && t >= 1) {
+                if (!wwait(bar(BAR_PV_DONE + ((t - 1) % kSPBufs)), ((t - 1) / kSPBufs) & 1)) return false;
+                __syncwarp();
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_base + kColO + c * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int v = 0; v < 32; ++v) o[v] = __float_as_uint(__uint_as_float(o[v]) * alpha);
+                    tmem_st32(tmem + lane_base + kColO + c * 32, o);
+                }
             }
+            // KV rows past the last node may hold anything (NaN included) and
+            // P is 0 there, but 0 * NaN is NaN: zero those V rows of the tail
+            // tile (S, which read them as K, is already complete)
+            const int key0 = (t0 + t) * kKeys;
+            if (key0 + kKeys > kend) {
+                uint4 *vset = reinterpret_cast<uint4 *>(smem + kOffRing + (t % kSlots) * kSlotBytes);
+                const int kvalid = kend - key0;
+#pragma unroll 1
+                for (int e = row; e < kQChunks * kChunkBytesKV / 16; e += kRows)
+                    if (((e >> 3) & (kKeys - 1)) >= kvalid) vset[e] = make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
+            }
+            tmem_st32(tmem + lane_base + kColSP + pb * 64, pk_hi);
+            tmem_st32(tmem + lane_base + kColSP + pb * 64 + 32, pk_lo);
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_S_FREE + sb));
-            // scale, mask, tile max
-            uint64_t vis = ~0ull;
-            if (!node_ok) vis = 0;
-            else if (key0 + kKeys > T) vis = tile_visibility(key0, T, n, m0, m1);
-            const uint32_t vis_lo = static_cast<uint32_t>(vis), vis_hi = static_cast<uint32_t>(vis >> 32);
-            float x[64];
-            float mx = -INFINITY;
+            if (lane == 0) mbar_arrive(bar(BAR_P_FULL + pb));
+            return true;
+        };
+
+        float m_ref = -INFINITY, l_sum = 0.f;
+        bool ok = true;
+        if (owner) {
+            // ---- own rows: add the partner's partial, softmax, ship P back
+            for (int jj = 0; jj < nt && ok; ++jj) {
+                const int key0 = (t0 + jj) * kKeys;
+                uint32_t sv[64];
+                if (!load_s(jj, sv)) {
+                    ok = false;
+                    break;
+                }
+                // one owner thread arms this tile's phase: 64 rows x 256 B
+                if (lr == 0) mbar_arrive_expect_tx(bar(BAR_SX_FULL), kSXBytes);
+                if (!wwait_cluster(bar(BAR_SX_FULL), jj & 1)) {
+                    ok = false;
+                    break;
+                }
+                float s[64];
 #pragma unroll
-            for (int k = 0; k < 64; ++k) {
-                const uint32_t bit = (k < 32 ? (vis_lo >> k) : (vis_hi >> (k - 32))) & 1u;
-                x[k] = bit ? __uint_as_float(sv[k]) * a.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, x[k]);
-            }
-            // P buffer sb was last read by PV of tile jj-2
-            if (jj >= 2 && !mbar_wait(bar(BAR_PV_DONE + sb), ((jj - 2) >> 1) & 1, deadline, abort_flag)) {
-                ok = false;
-                break;
-            }
-            const bool need = mx > m_ref + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, need)) {
-                const float alpha = need ? ex2_approx(m_ref - mx) : 1.0f;
-                if (need) {
+                for (int k4 = 0; k4 < 16; ++k4) {
+                    const uint4 o = sx[k4 * kOwnRows + lr];
+                    s[4 * k4] = __uint_as_float(sv[4 * k4]) + __uint_as_float(o.x);
+                    s[4 * k4 + 1] = __uint_as_float(sv[4 * k4 + 1]) + __uint_as_float(o.y);
+                    s[4 * k4 + 2] = __uint_as_float(sv[4 * k4 + 2]) + __uint_as_float(o.z);
+                    s[4 * k4 + 3] = __uint_as_float(sv[4 * k4 + 3]) + __uint_as_float(o.w);
+                }
+                mbar_arrive_remote(r_bar_sx_empty);
+                uint64_t vis = ~0ull;
+                if (!node_ok) vis = 0;
+                else if (key0 + kKeys > T) vis = tile_visibility(key0, T, n, m0, m1);
+                const uint32_t vis_lo = static_cast<uint32_t>(vis), vis_hi = static_cast<uint32_t>(vis >> 32);
+                float mx = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < 64; ++k) {
+                    const uint32_t bit = (k < 32 ? (vis_lo >> k) : (vis_hi >> (k - 32))) & 1u;
+                    s[k] = bit ? s[k] * a.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, s[k]);
+                }
+                float alpha = 1.0f;  // rescale factor of this row's O for this tile
+                if (mx > m_ref + kRescaleThreshold) {
+                    alpha = ex2_approx(m_ref - mx);  // 0 while nothing was visible before
                     m_ref = mx;
                     l_sum *= alpha;
                 }
-                if (jj >= 1) {
-                    // O must be quiescent: PV of tile jj-1 complete
-                    if (!mbar_wait(bar(BAR_PV_DONE + ((jj - 1) & 1)), ((jj - 1) >> 1) & 1, deadline, abort_flag)) {
+                // P = hi + lo, both bf16. While no key has been visible yet
+                // m_ref is -inf and every s is -inf: subtracting 0 keeps p = 0.
+                const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
+                uint32_t pk_hi[32], pk_lo[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const float p0 = ex2_approx(s[2 * k] - mref);
+                    const float p1 = ex2_approx(s[2 * k + 1] - mref);
+                    const uint32_t h = pack_bf16x2(p0, p1);
+                    pk_hi[k] = h;
+                    pk_lo[k] = pack_bf16x2(p0 - bf16lo_to_f32(h), p1 - bf16hi_to_f32(h));
+                    l_sum += p0 + p1;
+                }
+                // ship P and the rescale factor to the partner
+                if (jj >= 1 && !wwait_cluster(bar(BAR_PX_EMPTY), (jj - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int w4 = 0; w4 < 8; ++w4) {
+                    st_async_v4(r_px + (w4 * kOwnRows + lr) * 16,
+                                make_uint4(pk_hi[4 * w4], pk_hi[4 * w4 + 1], pk_hi[4 * w4 + 2], pk_hi[4 * w4 + 3]),
+                                r_bar_px_full);
+                    st_async_v4(r_px + ((w4 + 8) * kOwnRows + lr) * 16,
+                                make_uint4(pk_lo[4 * w4], pk_lo[4 * w4 + 1], pk_lo[4 * w4 + 2], pk_lo[4 * w4 + 3]),
+                                r_bar_px_full);
+                }
+                st_async_b32(r_ax + lr * 4, __float_as_uint(alpha), r_bar_px_full);
+                if (!publish(jj, alpha, pk_hi, pk_lo)) ok = false;
+            }
+        } else {
+            // ---- the partner's rows, one tile behind: ship tile jj's partial
+            // S first, then take tile jj-1's probabilities, so the round trip
+            // to the partner overlaps a whole tile
+            for (int jj = 0; jj <= nt && ok; ++jj) {
+                if (jj < nt) {
+                    uint32_t sv[64];
+                    if (!load_s(jj, sv)) {
                         ok = false;
                         break;
                     }
-                    __syncwarp();
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem + lane_base + kColO + c * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int v = 0; v < 32; ++v) o[v] = __float_as_uint(__uint_as_float(o[v]) * alpha);
-                        tmem_st32(tmem + lane_base + kColO + c * 32, o);
+                    if (jj >= 1 && !wwait_cluster(bar(BAR_SX_EMPTY), (jj - 1) & 1)) {
+                        ok = false;
+                        break;
                     }
-                    tmem_wait_st();
+#pragma unroll
+                    for (int k4 = 0; k4 < 16; ++k4)
+                        st_async_v4(r_sx + (k4 * kOwnRows + lr) * 16,
+                                    make_uint4(sv[4 * k4], sv[4 * k4 + 1], sv[4 * k4 + 2], sv[4 * k4 + 3]),
+                                    r_bar_sx_full);
+                }
+                if (jj >= 1) {
+                    const int t = jj - 1;
+                    // one helper thread arms the phase: 64 rows x 256 B of P + 64 factors
+                    if (lr == 0) mbar_arrive_expect_tx(bar(BAR_PX_FULL), kPXBytes + kOwnRows * 4);
+                    if (!wwait_cluster(bar(BAR_PX_FULL), t & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    uint32_t pk_hi[32], pk_lo[32];
+#pragma unroll
+                    for (int w4 = 0; w4 < 8; ++w4) {
+                        const uint4 h = px[w4 * kOwnRows + lr];
+                        const uint4 l = px[(w4 + 8) * kOwnRows + lr];
+                        pk_hi[4 * w4] = h.x;
+                        pk_hi[4 * w4 + 1] = h.y;
+                        pk_hi[4 * w4 + 2] = h.z;
+                        pk_hi[4 * w4 + 3] = h.w;
+                        pk_lo[4 * w4] = l.x;
+                        pk_lo[4 * w4 + 1] = l.y;
+                        pk_lo[4 * w4 + 2] = l.z;
+                        pk_lo[4 * w4 + 3] = l.w;
+                    }
+                    const float alpha = ax[lr];
+                    if (!publish(t, alpha, pk_hi, pk_lo)) ok = false;
+                    // the values read from PX are in tensor memory now
+                    // (publish waited for its tcgen05.st), so the buffer can
+                    // be handed back without a release, which would also wait
+                    // for this thread's st.async of tile jj
+                    mbar_arrive_remote_relaxed(r_bar_px_empty);
                 }
             }
-            // probabilities (fp16) into tensor memory. While no key has been
-            // visible yet m_ref is -inf and every x is -inf: subtracting 0
-            // instead keeps p = 0 without a per-element test. The row sum
-            // adds the fp32 values (fp16 rounding is unbiased, 2^-11 each).
-            uint32_t pk[32];
-            const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const float p0 = ex2_approx(x[2 * k] - mref);
-                const float p1 = ex2_approx(x[2 * k + 1] - mref);
-                pk[k] = pack_f16x2(p0, p1);
-                l_sum += p0 + p1;
-            }
-            tmem_st32(tmem + lane_base + kColP + sb * 32, pk);
-            // S of this tile is complete, so its V chunks (read as bf16 K by
-            // S) can turn into the fp16 B operand of PV, in place. KV rows
-            // past the last node may hold anything (NaN included): they become
-            // zeros so that 0 * garbage cannot reach O.
-            {
-                uint4 *vset = reinterpret_cast<uint4 *>(smem + kOffV + sb * kVSetBytes);
-                const int kvalid = kend - key0;  // keys of this tile that exist
-#pragma unroll 1
-                for (int e0 = row; e0 < kVSetBytes / 16; e0 += 4 * kRows) {
-                    uint4 v[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) v[u] = vset[e0 + u * kRows];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int key = ((e0 + u * kRows) >> 3) & (kKeys - 1);  // 8 units of 16 B per key row
-                        if (key < kvalid) {
-                            v[u].x = bf16x2_to_f16x2(v[u].x);
-                            v[u].y = bf16x2_to_f16x2(v[u].y);
-                            v[u].z = bf16x2_to_f16x2(v[u].z);
-                            v[u].w = bf16x2_to_f16x2(v[u].w);
-                        } else {
-                            v[u] = make_uint4(0, 0, 0, 0);
-                        }
-                        vset[e0 + u * kRows] = v[u];
-                    }
-                }
-                fence_proxy_async_smem();
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_P_FULL + sb));
         }
-        if (ok && !mbar_wait(bar(BAR_O_FINAL), 0, deadline, abort_flag)) ok = false;
+        if (ok && !wwait(bar(BAR_O_FINAL), 0)) ok = false;
+        // final row sums: owners hand theirs to the partner's other half
+        if (ok && owner) st_async_b32(r_lx + lr * 4, __float_as_uint(l_sum), r_bar_lx_full);
+        if (ok && !owner) {
+            if (lr == 0) mbar_arrive_expect_tx(bar(BAR_LX_FULL), kOwnRows * 4);
+            if (!wwait_cluster(bar(BAR_LX_FULL), 0)) ok = false;
+            else l_sum = lx[lr];
+        }
         if (!ok) {
             fail();
         } else {
             __syncwarp();
             tc_fence_after();
             const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-            float *dst = o_dst + (row_base + g) * 512 + half * 256;
+            float *dst = o_dst + (row_base + g) * 512 + rank * 256;
 #pragma unroll 1
             for (int c = 0; c < 8; ++c) {
                 uint32_t o[32];
@@ -561,13 +663,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             __uint_as_float(o[4 * v + 3]) * inv_l);
                 }
             }
-            if (half == 0 && row_in_seq)
+            if (owner && row_in_seq)
                 lse_dst[row_base + g] = l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
         }
     }
 
     tc_fence_before();
-    __syncthreads();
+    // neither CTA may leave while its partner can still write into it
+    cluster_sync();
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -628,15 +731,16 @@ EncodeTiledFn get_encoder() {
     return fn;
 }
 
+// bf16 matrix [rows, cols] row-major, box [box_rows, box_cols]
 bool encode_2d(EncodeTiledFn enc, CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows,
-               uint32_t box_cols, uint32_t box_rows) {
+               uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -644,20 +748,30 @@ bool encode_2d(EncodeTiledFn enc, CUtensorMap *m, const void *ptr, uint64_t cols
 AttnPlan plan_attention(int B, int Qc, int H, int Tcap, int sms) {
     AttnPlan p{};
     p.mtiles = (Qc * H + kRows - 1) / kRows;
+    // each row tile is a cluster of two CTAs, one per SM
     const long long base = static_cast<long long>(B) * p.mtiles * 2;
-    const int tiles_max = (Tcap + kKeys - 1) / kKeys;
-    int nsplit = 1;
-    if (base < 2LL * sms) {
-        // spread the key range until the grid covers the GPU about twice, but
-        // keep at least 4 key tiles per chunk
-        nsplit = static_cast<int>((2LL * sms + base - 1) / base);
-        const int max_split = tiles_max / 4 > 1 ? tiles_max / 4 : 1;
-        if (nsplit > max_split) nsplit = max_split;
-        if (nsplit < 1) nsplit = 1;
-    }
-    p.nsplit = nsplit;
+    const int tiles = (Tcap + kKeys - 1) / kKeys;
     const size_t rows_total = static_cast<size_t>(B) * Qc * H;
-    p.ws_bytes = nsplit > 1 ? static_cast<size_t>(nsplit) * rows_total * (512 + 1) * sizeof(float) : 0;
+    // Pick the split of each sequence's keys that minimises a simple cost:
+    // waves of CTAs x key tiles per CTA (about 1 us each, plus 2 for the
+    // prologue and epilogue), plus the partial outputs the merge writes and
+    // reads (about 1 us per 4 MB at HBM rate). At least 4 key tiles per range.
+    int best = 1;
+    double best_cost = 1e30;
+    const int max_split = tiles / 4 > 1 ? tiles / 4 : 1;
+    for (int s = 1; s <= max_split && s <= 64; ++s) {
+        const long long ctas = base * s;
+        const long long waves = (ctas + sms - 1) / sms;
+        const double per_cta = static_cast<double>((tiles + s - 1) / s) + 2.0;
+        const double merge = s > 1 ? static_cast<double>(s + 1) * rows_total * 2048.0 / 4.0e6 : 0.0;
+        const double cost = waves * per_cta + merge;
+        if (cost < best_cost * 0.98) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    p.nsplit = best;
+    p.ws_bytes = best > 1 ? static_cast<size_t>(best) * rows_total * (512 + 1) * sizeof(float) : 0;
     return p;
 }
 
@@ -669,9 +783,9 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
     const uint64_t rows_total = static_cast<uint64_t>(tree.B) * tree.Qc * in.H;
     const uint64_t kv_rows = static_cast<uint64_t>(tree.B) * in.Tcap;
     CUtensorMap tm_q, tm_kv, tm_kr;
-    if (!encode_2d(enc, &tm_q, in.q_lat, 512, rows_total, 64, kRows) ||
-        !encode_2d(enc, &tm_kv, in.c_kv, 512, kv_rows, 64, kKeys) ||
-        !encode_2d(enc, &tm_kr, in.k_rope, 64, kv_rows, 64, kKeys))
+    if (!encode_2d(enc, &tm_q, in.q_lat, 512, rows_total, 64, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(enc, &tm_kv, in.c_kv, 512, kv_rows, 64, kKeys, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(enc, &tm_kr, in.k_rope, 64, kv_rows, 32, kKeys, CU_TENSOR_MAP_SWIZZLE_64B))
         return DDT_E_INVAL;
 
     static std::once_flag attr_once;
@@ -692,6 +806,7 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
     a.mask = tree.mask;
     a.n_nodes = tree.n_nodes;
     a.prefix_len = in.prefix_len;
+    a.q_lat = static_cast<const uint16_t *>(in.q_lat);
     a.q_rope = static_cast<const uint16_t *>(in.q_rope);
     a.status = tree.status;
     a.rows_total = rows_total;
