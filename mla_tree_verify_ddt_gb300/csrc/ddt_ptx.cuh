@@ -146,6 +146,20 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) 
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 
+// The same, issued only once `dep` is available: pass a value computed from
+// every word read out of the buffer being handed back. `dep` is first stored
+// to a scratch word (a side effect that cannot be dropped, and that cannot
+// issue before all those loads have returned), and instructions issue in
+// order, so the arrive cannot overtake the loads.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed_after(uint32_t remote_bar, uint32_t dep,
+                                                                 uint32_t scratch_smem) {
+    asm volatile(
+        "st.shared.u32 [%2], %1;\n\t"
+        "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar),
+        "r"(dep), "r"(scratch_smem)
+        : "memory");
+}
+
 // Whole-cluster barrier (every thread of every CTA of the cluster).
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");

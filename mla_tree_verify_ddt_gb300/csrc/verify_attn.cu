@@ -206,6 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t sBar = sbase + kOffBar;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + NUM_BARS * 8 + 4);
+    // (the word after it is a scratch target for dependency stores)
     auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
 
     if (tid == 0) {
@@ -326,6 +327,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 pv_next += r;
                 return true;
             };
+            // Wait for a barrier phase, issuing any PV (up to tile `upto`)
+            // whose P becomes ready meanwhile: the ring and the S/P buffers
+            // are freed by PVs, so an idle issuer must not sit on a ready one.
+            auto wait_feeding_pv = [&](uint32_t barrier, uint32_t parity, int upto) -> bool {
+                for (uint32_t it = 0;; ++it) {
+                    if (mbar_try_wait(barrier, parity)) return true;
+                    if (pv_next < upto && pv_next < nt) {
+                        const int r = issue_pv(pv_next, false);
+                        if (r < 0) return false;
+                        pv_next += r;
+                    }
+                    if ((it & 63u) == 63u && (*abort_flag || globaltimer_ns() > deadline)) return false;
+                }
+            };
             for (int jj = 0; jj < nt && ok; ++jj) {
                 const int sb = jj % kSPBufs, slot = jj % kSlots;
                 // a PV that became ready goes first
@@ -334,12 +349,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 // the S/P buffer of tile jj-3 is free once its PV is done
-                if (jj >= kSPBufs &&
-                    !mbar_wait(bar(BAR_PV_DONE + sb), ((jj - kSPBufs) / kSPBufs) & 1, deadline, abort_flag)) {
+                if (jj >= kSPBufs && !wait_feeding_pv(bar(BAR_PV_DONE + sb), ((jj - kSPBufs) / kSPBufs) & 1, jj)) {
                     ok = false;
                     break;
                 }
-                if (!mbar_wait(bar(BAR_RING_FULL + slot), (jj / kSlots) & 1, deadline, abort_flag)) {
+                if (!wait_feeding_pv(bar(BAR_RING_FULL + slot), (jj / kSlots) & 1, jj)) {
                     ok = false;
                     break;
                 }
@@ -525,15 +539,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 float s[64];
+                uint32_t read_dep = 0;  // depends on every word read from SX
 #pragma unroll
                 for (int k4 = 0; k4 < 16; ++k4) {
                     const uint4 o = sx[k4 * kOwnRows + lr];
+                    read_dep ^= o.x ^ o.y ^ o.z ^ o.w;
                     s[4 * k4] = __uint_as_float(sv[4 * k4]) + __uint_as_float(o.x);
                     s[4 * k4 + 1] = __uint_as_float(sv[4 * k4 + 1]) + __uint_as_float(o.y);
                     s[4 * k4 + 2] = __uint_as_float(sv[4 * k4 + 2]) + __uint_as_float(o.z);
                     s[4 * k4 + 3] = __uint_as_float(sv[4 * k4 + 3]) + __uint_as_float(o.w);
                 }
-                mbar_arrive_remote(r_bar_sx_empty);
+                // hand the partner's buffer back once every read of it is done
+                // (the arrive waits for read_dep); a release would also wait
+                // for this thread's st.async of the previous tile's P
+                mbar_arrive_remote_relaxed_after(r_bar_sx_empty, read_dep, sBar + NUM_BARS * 8 + 8);
                 uint64_t vis = ~0ull;
                 if (!node_ok) vis = 0;
                 else if (key0 + kKeys > T) vis = tile_visibility(key0, T, n, m0, m1);
