@@ -29,6 +29,7 @@ namespace {
 constexpr int kFrontierSlots = 3;  // per lane: 96 >= budget + 1
 constexpr int kWarpsPerBlock = 4;
 constexpr int kMaxQc = DDT_MAX_BUDGET + 1;
+constexpr int kMaxDK = DDT_MAX_DEPTH * DDT_MAX_TOPK;
 
 // Sort key: smaller is selected first.
 struct Key {
@@ -48,6 +49,10 @@ __device__ __forceinline__ bool key_less(const Key &a, const Key &b) {
 }
 
 struct WarpSmem {
+    // the sequence's drafter rows, staged once so that the pops, which form
+    // one dependent chain, never wait on global memory
+    float d_lp[kMaxDK];
+    int d_tok[kMaxDK];
     // frontier, slot = lane * kFrontierSlots + k
     float f_score[32 * kFrontierSlots];
     uint64_t f_path[32 * kFrontierSlots];
@@ -84,14 +89,18 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     // tokens in range) and the root token
     bool bad = false;
     for (int e = lane; e < D * K; e += 32) {
-        float v = lp[e];
-        int t = tok[e];
+        const float v = lp[e];
+        const int t = tok[e];
+        sm.d_lp[e] = v;
+        sm.d_tok[e] = t;
         if (isnan(v) || v > 0.0f) bad = true;
-        if ((e % K) > 0 && v > lp[e - 1]) bad = true;
         if (t < 0 || t >= vocab) bad = true;
     }
     const int32_t root = root_tok[b];
     if (root < 0 || root >= vocab) bad = true;
+    __syncwarp();
+    for (int e = lane; e < D * K; e += 32)
+        if ((e % K) > 0 && sm.d_lp[e] > sm.d_lp[e - 1]) bad = true;
     bad = __any_sync(0xffffffffu, bad);
 
     for (int k = 0; k < kFrontierSlots; ++k) sm.f_valid[lane * kFrontierSlots + k] = 0;
@@ -105,7 +114,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
         sm.n_mask[0][1] = 0ull;
         // the only initial candidate: depth 1, rank 0
         sm.f_valid[0] = 1;
-        sm.f_score[0] = __fadd_rn(0.0f, lp[0]);
+        sm.f_score[0] = __fadd_rn(0.0f, sm.d_lp[0]);
         sm.f_path[0] = 0ull;
         sm.f_depth[0] = 1;
         sm.f_parent[0] = 0;
@@ -142,43 +151,50 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
             if (best_slot < 0) break;  // frontier empty
             const float s = sm.f_score[best_slot];
             if (s == -INFINITY) break;  // everything left is -inf
+            const int d = sm.f_depth[best_slot];
+            const uint64_t path = sm.f_path[best_slot];
+            const int pnode = sm.f_parent[best_slot];
+            const int shift = 4 * (16 - d);
+            const int r = static_cast<int>((path >> shift) & 15ull);
+            const bool has_sibling = r + 1 < K;
+            const bool has_child = d < D;
+            // the popped slot becomes the next sibling (same parent, rank r+1);
+            // the first child (depth d+1, rank 0) takes the popped slot when
+            // there is no sibling, else the lowest free slot, found by the warp
+            int child_slot = best_slot;
+            if (has_child && has_sibling) {
+                int mine = 0x7fffffff;
+                for (int k = 0; k < kFrontierSlots; ++k)
+                    if (!sm.f_valid[lane * kFrontierSlots + k]) {
+                        mine = lane * kFrontierSlots + k;
+                        break;
+                    }
+                for (int off = 16; off > 0; off >>= 1) mine = min(mine, __shfl_xor_sync(0xffffffffu, mine, off));
+                child_slot = mine;  // exists: at most budget+1 <= 65 live entries
+            }
+            __syncwarp();
             if (lane == 0) {
-                const int d = sm.f_depth[best_slot];
-                const uint64_t path = sm.f_path[best_slot];
-                const int pnode = sm.f_parent[best_slot];
-                const int shift = 4 * (16 - d);
-                const int r = static_cast<int>((path >> shift) & 15ull);
                 const int i = n;
                 sm.n_score[i] = s;
                 sm.n_parent[i] = pnode;
                 sm.n_depth[i] = d;
                 sm.n_rank[i] = r;
-                sm.n_token[i] = tok[(d - 1) * K + r];
+                sm.n_token[i] = sm.d_tok[(d - 1) * K + r];
                 sm.n_mask[i][0] = sm.n_mask[pnode][0];
                 sm.n_mask[i][1] = sm.n_mask[pnode][1];
                 sm.n_mask[i][i >> 6] |= 1ull << (i & 63);
-                // the popped slot becomes the next sibling (same parent,
-                // rank r+1) or is freed
-                if (r + 1 < K) {
-                    sm.f_score[best_slot] = __fadd_rn(sm.n_score[pnode], lp[(d - 1) * K + r + 1]);
+                if (has_sibling) {
+                    sm.f_score[best_slot] = __fadd_rn(sm.n_score[pnode], sm.d_lp[(d - 1) * K + r + 1]);
                     sm.f_path[best_slot] = path + (1ull << shift);
-                } else {
+                } else if (!has_child) {
                     sm.f_valid[best_slot] = 0;
                 }
-                // first child (depth d+1, rank 0) into any free slot
-                if (d < D) {
-                    int free_slot = -1;
-                    for (int q = 0; q < 32 * kFrontierSlots; ++q)
-                        if (!sm.f_valid[q]) {
-                            free_slot = q;
-                            break;
-                        }
-                    // free_slot always exists: at most budget+1 <= 65 live entries
-                    sm.f_valid[free_slot] = 1;
-                    sm.f_score[free_slot] = __fadd_rn(s, lp[d * K + 0]);
-                    sm.f_path[free_slot] = path;
-                    sm.f_depth[free_slot] = d + 1;
-                    sm.f_parent[free_slot] = i;
+                if (has_child) {
+                    sm.f_valid[child_slot] = 1;
+                    sm.f_score[child_slot] = __fadd_rn(s, sm.d_lp[d * K + 0]);
+                    sm.f_path[child_slot] = path;
+                    sm.f_depth[child_slot] = d + 1;
+                    sm.f_parent[child_slot] = i;
                 }
             }
             ++n;

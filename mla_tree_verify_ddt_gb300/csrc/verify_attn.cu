@@ -87,8 +87,9 @@ constexpr int kOffPX = kOffSX + kSXBytes;                         // 212992: par
 constexpr int kPXBytes = kOwnRows * kKeys * 4;                    // 16384 (32 hi + 32 lo words per row)
 constexpr int kOffAX = kOffPX + kPXBytes;                         // 229376: rescale factor per row
 constexpr int kOffLX = kOffAX + kOwnRows * 4;                     // 229632: final row sum per row
-constexpr int kOffBar = kOffLX + kOwnRows * 4;                    // 229888
-constexpr int kSmemBytes = kOffBar + 256 + 1024;                  // + alignment slack
+constexpr int kOffBar = kOffLX + kOwnRows * 4;                    // 229888: barriers and flags (256 B)
+constexpr int kOffMX = kOffBar + 256;                             // 230144: [2 rounds][2 key halves][64 rows]
+constexpr int kSmemBytes = kOffMX + 2 * 2 * kOwnRows * 4 + 1024;  // + alignment slack
 
 // tensor memory columns
 constexpr uint32_t kColO = 0;       // 256: this CTA's half of O
@@ -99,7 +100,9 @@ constexpr uint32_t kColQR = 480;    // 16: rotary query (bf16 pairs)
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kThreads = 192;  // warps 0-3 softmax group, 4 TMA producer, 5 MMA issuer
+// warps 0-7 softmax group (two threads per row), 8 TMA producer, 9 MMA issuer
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 
 enum {
     BAR_Q_FULL = 0,
@@ -117,7 +120,10 @@ enum {
     BAR_PX_FULL = 23,    // partner wrote P for my other rows into my PX
     BAR_PX_EMPTY = 24,   // partner read the P I wrote into its PX
     BAR_LX_FULL = 25,    // partner wrote final row sums into my LX
-    NUM_BARS = 26
+    // the two threads of an owned row swap their halves' tile max (and, at
+    // the end, their row sums): one barrier per owned TMEM quadrant
+    BAR_MAXX = 26,       // 2
+    NUM_BARS = 28
 };
 
 struct AttnArgs {
@@ -135,15 +141,15 @@ struct AttnArgs {
     unsigned long long wait_ns;
 };
 
-// Visibility of keys key0..key0+63 for a node with ancestor mask (m0, m1):
-// every prefix key (< T) and the keys T+m of ancestors-or-self m < n. Only
-// tiles that reach past the prefix need it; the loop stays rolled to keep
-// the softmax code small (a fully unrolled per-key test made the softmax
-// warps wait on instruction fetch).
-__device__ __noinline__ uint64_t tile_visibility(int key0, int T, int n, uint64_t m0, uint64_t m1) {
-    uint64_t vis = 0;
+// Visibility of keys key0..key0+31 (half a tile) for a node with ancestor
+// mask (m0, m1): every prefix key (< T) and the keys T+m of ancestors-or-self
+// m < n. Only tiles that reach past the prefix need it; the loop stays rolled
+// to keep the softmax code small (a fully unrolled per-key test made the
+// softmax warps wait on instruction fetch).
+__device__ __noinline__ uint32_t half_tile_visibility(int key0, int T, int n, uint64_t m0, uint64_t m1) {
+    uint32_t vis = 0;
 #pragma unroll 1
-    for (int k = 0; k < 64; ++k) {
+    for (int k = 0; k < 32; ++k) {
         const int key = key0 + k;
         bool v;
         if (key < T) {
@@ -152,7 +158,7 @@ __device__ __noinline__ uint64_t tile_visibility(int key0, int T, int n, uint64_
             const int m = key - T;
             v = m < n && (((m < 64 ? m0 : m1) >> (m & 63)) & 1ull);
         }
-        vis |= static_cast<uint64_t>(v) << k;
+        vis |= static_cast<uint32_t>(v) << k;
     }
     return vis;
 }
@@ -211,14 +217,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(bar(BAR_Q_FULL), 1);
-        mbar_init(bar(BAR_QT_READY), 4);
+        mbar_init(bar(BAR_QT_READY), 8);
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(bar(BAR_RING_FULL + s), 1);
             mbar_init(bar(BAR_RING_EMPTY + s), 1);
         }
         for (int s = 0; s < kSPBufs; ++s) {
             mbar_init(bar(BAR_S_FULL + s), 1);
-            mbar_init(bar(BAR_P_FULL + s), 4);
+            mbar_init(bar(BAR_P_FULL + s), 8);
             mbar_init(bar(BAR_PV_DONE + s), 1);
         }
         mbar_init(bar(BAR_O_FINAL), 1);
@@ -226,14 +232,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // the FULL barriers complete on bytes: one local thread arms each
         // phase with expect_tx and the partner's st.async credits the bytes
         mbar_init(bar(BAR_SX_FULL), 1);
-        mbar_init(bar(BAR_SX_EMPTY), kOwnRows);
+        mbar_init(bar(BAR_SX_EMPTY), 2 * kOwnRows);
         mbar_init(bar(BAR_PX_FULL), 1);
-        mbar_init(bar(BAR_PX_EMPTY), kOwnRows);
+        mbar_init(bar(BAR_PX_EMPTY), 2 * kOwnRows);
+        mbar_init(bar(BAR_MAXX), 64);
+        mbar_init(bar(BAR_MAXX + 1), 64);
         mbar_init(bar(BAR_LX_FULL), 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -249,7 +257,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         a.status[b] = DDT_E_TIMEOUT;
     };
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ======================= TMA producer =======================
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
@@ -288,7 +296,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (armed[s]) mbar_wait(bar(BAR_RING_FULL + s), (armed[s] - 1) & 1, drain_deadline, &zero);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ======================= MMA issuer =======================
         if (lane == 0) {
             constexpr uint32_t idS = idesc_f32acc(kRows, kKeys, 1, 0, 0);   // bf16 Q, K (K-major)
@@ -309,13 +317,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int slot = j % kSlots;
                 const uint32_t vb = sRing + slot * kSlotBytes;
+                // keys 32c..32c+31 of P sit in columns 32c..32c+31 of the
+                // buffer: 16 hi words, then 16 lo words
                 const uint32_t pcol = tmem + kColSP + pb * 64;
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    mma_ts(tmem + kColO, pcol + ks * 8, desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV,
-                           (j > 0 || ks > 0) ? 1u : 0u);
+                    mma_ts(tmem + kColO, pcol + (ks >> 1) * 32 + (ks & 1) * 8,
+                           desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV, (j > 0 || ks > 0) ? 1u : 0u);
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    mma_ts(tmem + kColO, pcol + 32 + ks * 8, desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV,
-                           1u);
+                    mma_ts(tmem + kColO, pcol + (ks >> 1) * 32 + 16 + (ks & 1) * 8,
+                           desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV, 1u);
                 mma_commit(bar(BAR_PV_DONE + pb));
                 mma_commit(bar(BAR_RING_EMPTY + slot));
                 return 1;
@@ -395,25 +405,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ======================= softmax group (warps 0-3) =======================
-        const int row = warp * 32 + lane;            // TMEM lane of this thread
+        // ======================= softmax group (warps 0-7) =======================
+        // Warp w serves tensor-memory lanes 32(w%4)..+31 (one row per lane)
+        // and key half c = w/4 of every tile: keys [32c, 32c+32). The two
+        // threads of a row agree on the row max through shared memory once
+        // per tile and add their row sums at the end.
+        const int quad = warp & 3, half = warp >> 2;
+        const int row = quad * 32 + lane;            // TMEM lane of this thread
         const bool owner = (row >> 6) == static_cast<int>(rank);
         const int lr = row & (kOwnRows - 1);         // row index within its 64-row half
         const int g = mt * kRows + row;              // row within the sequence
         const bool row_in_seq = g < rows_seq;
         const int node = g / a.H;
         const bool node_ok = row_in_seq && node < n && seq_ok;
+        const bool lead = lr == 0 && half == 0;      // arms the exchange barriers' byte counts
         uint64_t m0 = 0, m1 = 0;
         if (owner && node_ok) {
             const uint64_t *mk = a.mask + (static_cast<size_t>(b) * a.Qc + node) * a.W;
             m0 = mk[0];
             if (a.W > 1) m1 = mk[1];
         }
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t col_half = static_cast<uint32_t>(half) * 32;   // this thread's 32 columns of an S/P buffer
         const uint4 *sx = reinterpret_cast<const uint4 *>(smem + kOffSX);   // [16][64 rows] of 4 floats
         const uint4 *px = reinterpret_cast<const uint4 *>(smem + kOffPX);   // [16][64 rows] of 4 words
         const volatile float *ax = reinterpret_cast<const volatile float *>(smem + kOffAX);
         const volatile float *lx = reinterpret_cast<const volatile float *>(smem + kOffLX);
+        volatile float *mx_x = reinterpret_cast<volatile float *>(smem + kOffMX);  // [2][2][64]
         // the partner's copies of the exchange buffers and barriers
         const uint32_t r_sx = mapa_shared(sbase + kOffSX, peer);
         const uint32_t r_px = mapa_shared(sbase + kOffPX, peer);
@@ -424,6 +442,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t r_bar_px_full = mapa_shared(bar(BAR_PX_FULL), peer);
         const uint32_t r_bar_px_empty = mapa_shared(bar(BAR_PX_EMPTY), peer);
         const uint32_t r_bar_lx_full = mapa_shared(bar(BAR_LX_FULL), peer);
+        // SX / PX hold a row's 64 words as 16 groups of 4; this half's are groups 8c..8c+7
+        const int grp0 = half * 8;
 
         // waits of the softmax group are made warp-uniform, so a lane that
         // gives up can never leave its warp split before a .sync.aligned op
@@ -433,71 +453,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto wwait_cluster = [&](uint32_t barrier, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait_cluster(barrier, parity, deadline, abort_flag));
         };
+        // The two threads of an owned row swap one float through shared
+        // memory: round k uses buffer k&1 and phase k of the quadrant's barrier.
+        auto swap_with_other_half = [&](int k, float v, float &other) -> bool {
+            mx_x[((k & 1) * 2 + half) * kOwnRows + lr] = v;
+            mbar_arrive(bar(BAR_MAXX + (quad & 1)));
+            if (!wwait(bar(BAR_MAXX + (quad & 1)), k & 1)) return false;
+            other = mx_x[((k & 1) * 2 + (half ^ 1)) * kOwnRows + lr];
+            return true;
+        };
 
-        // this row's latent query chunk 3 and rotary query -> tensor memory,
-        // as bf16 pairs (low half = even column)
+        // this row's latent query chunk 3 (key-half-0 warps) or rotary query
+        // (key-half-1 warps) -> tensor memory, as bf16 pairs (low half = even column)
         {
-            uint32_t q3[32], qr[32];
+            uint32_t q[32];
 #pragma unroll
-            for (int v = 0; v < 32; ++v) q3[v] = qr[v] = 0;
+            for (int v = 0; v < 32; ++v) q[v] = 0;
             if (row_in_seq) {
-                const uint4 *s3 = reinterpret_cast<const uint4 *>(a.q_lat + (row_base + g) * 512 + rank * 256 + 192);
-                const uint4 *sr = reinterpret_cast<const uint4 *>(a.q_rope + (row_base + g) * 64 + rank * 32);
+                const uint4 *src =
+                    half == 0 ? reinterpret_cast<const uint4 *>(a.q_lat + (row_base + g) * 512 + rank * 256 + 192)
+                              : reinterpret_cast<const uint4 *>(a.q_rope + (row_base + g) * 64 + rank * 32);
+                const int nv = half == 0 ? 8 : 4;
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
-                    const uint4 x = s3[v];
-                    q3[4 * v] = x.x;
-                    q3[4 * v + 1] = x.y;
-                    q3[4 * v + 2] = x.z;
-                    q3[4 * v + 3] = x.w;
-                }
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const uint4 x = sr[v];
-                    qr[4 * v] = x.x;
-                    qr[4 * v + 1] = x.y;
-                    qr[4 * v + 2] = x.z;
-                    qr[4 * v + 3] = x.w;
+                    if (v < nv) {
+                        const uint4 x = src[v];
+                        q[4 * v] = x.x;
+                        q[4 * v + 1] = x.y;
+                        q[4 * v + 2] = x.z;
+                        q[4 * v + 3] = x.w;
+                    }
                 }
             }
-            tmem_st32(tmem + lane_base + kColQ3, q3);
-            tmem_st16(tmem + lane_base + kColQR, *reinterpret_cast<const uint32_t(*)[16]>(&qr[0]));
+            if (half == 0) tmem_st32(tmem + lane_base + kColQ3, q);
+            else tmem_st16(tmem + lane_base + kColQR, *reinterpret_cast<const uint32_t(*)[16]>(&q[0]));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(BAR_QT_READY));
         }
 
-        // this thread's row of the partial S of tile t, from tensor memory
-        auto load_s = [&](int t, uint32_t (&sv)[64]) -> bool {
+        // this thread's 32 keys of the partial S of tile t, from tensor memory
+        auto load_s = [&](int t, uint32_t (&sv)[32]) -> bool {
             const int sb = t % kSPBufs;
             if (!wwait(bar(BAR_S_FULL + sb), (t / kSPBufs) & 1)) return false;
             __syncwarp();
             tc_fence_after();
-            uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-            uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-            tmem_ld32(tmem + lane_base + kColSP + sb * 64, lo);
-            tmem_ld32(tmem + lane_base + kColSP + sb * 64 + 32, hi);
+            tmem_ld32(tmem + lane_base + kColSP + sb * 64 + col_half, sv);
             tmem_wait_ld();
             return true;
         };
-        // P of tile t for this row into this CTA's tensor memory, over the
-        // row's own (already read) S of that tile, after the row's O has been
-        // rescaled by alpha; the rescale needs O quiescent (PV of t-1 done)
-        auto publish = [&](int t, float alpha, const uint32_t (&pk_hi)[32], const uint32_t (&pk_lo)[32]) -> bool {
+        // P of tile t for this thread's 32 keys (16 hi words, then 16 lo
+        // words) into this CTA's tensor memory, over the thread's own (already
+        // read) S columns, after the row's O half has been rescaled by alpha;
+        // the rescale needs O quiescent (PV of t-1 done)
+        auto publish = [&](int t, float alpha, const uint32_t (&pw)[32]) -> bool {
             const int pb = t % kSPBufs;
             if (__any_sync(0xffffffffu, alpha != 1.0f) && t >= 1) {
                 if (!wwait(bar(BAR_PV_DONE + ((t - 1) % kSPBufs)), ((t - 1) / kSPBufs) & 1)) return false;
                 __syncwarp();
                 tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t col = kColO + half * 128 + c * 32;
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + kColO + c * 32, o);
+                    tmem_ld32(tmem + lane_base + col, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int v = 0; v < 32; ++v) o[v] = __float_as_uint(__uint_as_float(o[v]) * alpha);
-                    tmem_st32(tmem + lane_base + kColO + c * 32, o);
+                    tmem_st32(tmem + lane_base + col, o);
                 }
             }
             // KV rows past the last node may hold anything (NaN included) and
@@ -508,12 +532,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 uint4 *vset = reinterpret_cast<uint4 *>(smem + kOffRing + (t % kSlots) * kSlotBytes);
                 const int kvalid = kend - key0;
 #pragma unroll 1
-                for (int e = row; e < kQChunks * kChunkBytesKV / 16; e += kRows)
+                for (int e = half * kRows + row; e < kQChunks * kChunkBytesKV / 16; e += 2 * kRows)
                     if (((e >> 3) & (kKeys - 1)) >= kvalid) vset[e] = make_uint4(0, 0, 0, 0);
                 fence_proxy_async_smem();
             }
-            tmem_st32(tmem + lane_base + kColSP + pb * 64, pk_hi);
-            tmem_st32(tmem + lane_base + kColSP + pb * 64 + 32, pk_lo);
+            tmem_st32(tmem + lane_base + kColSP + pb * 64 + col_half, pw);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -526,44 +549,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (owner) {
             // ---- own rows: add the partner's partial, softmax, ship P back
             for (int jj = 0; jj < nt && ok; ++jj) {
-                const int key0 = (t0 + jj) * kKeys;
-                uint32_t sv[64];
+                const int key0 = (t0 + jj) * kKeys + half * 32;
+                uint32_t sv[32];
                 if (!load_s(jj, sv)) {
                     ok = false;
                     break;
                 }
                 // one owner thread arms this tile's phase: 64 rows x 256 B
-                if (lr == 0) mbar_arrive_expect_tx(bar(BAR_SX_FULL), kSXBytes);
+                if (lead) mbar_arrive_expect_tx(bar(BAR_SX_FULL), kSXBytes);
                 if (!wwait_cluster(bar(BAR_SX_FULL), jj & 1)) {
                     ok = false;
                     break;
                 }
-                float s[64];
+                float s[32];
                 uint32_t read_dep = 0;  // depends on every word read from SX
 #pragma unroll
-                for (int k4 = 0; k4 < 16; ++k4) {
-                    const uint4 o = sx[k4 * kOwnRows + lr];
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 o = sx[(grp0 + i) * kOwnRows + lr];
                     read_dep ^= o.x ^ o.y ^ o.z ^ o.w;
-                    s[4 * k4] = __uint_as_float(sv[4 * k4]) + __uint_as_float(o.x);
-                    s[4 * k4 + 1] = __uint_as_float(sv[4 * k4 + 1]) + __uint_as_float(o.y);
-                    s[4 * k4 + 2] = __uint_as_float(sv[4 * k4 + 2]) + __uint_as_float(o.z);
-                    s[4 * k4 + 3] = __uint_as_float(sv[4 * k4 + 3]) + __uint_as_float(o.w);
+                    s[4 * i] = __uint_as_float(sv[4 * i]) + __uint_as_float(o.x);
+                    s[4 * i + 1] = __uint_as_float(sv[4 * i + 1]) + __uint_as_float(o.y);
+                    s[4 * i + 2] = __uint_as_float(sv[4 * i + 2]) + __uint_as_float(o.z);
+                    s[4 * i + 3] = __uint_as_float(sv[4 * i + 3]) + __uint_as_float(o.w);
                 }
                 // hand the partner's buffer back once every read of it is done
                 // (the arrive waits for read_dep); a release would also wait
                 // for this thread's st.async of the previous tile's P
                 mbar_arrive_remote_relaxed_after(r_bar_sx_empty, read_dep, sBar + NUM_BARS * 8 + 8);
-                uint64_t vis = ~0ull;
+                uint32_t vis = ~0u;
                 if (!node_ok) vis = 0;
-                else if (key0 + kKeys > T) vis = tile_visibility(key0, T, n, m0, m1);
-                const uint32_t vis_lo = static_cast<uint32_t>(vis), vis_hi = static_cast<uint32_t>(vis >> 32);
+                else if (key0 + 32 > T) vis = half_tile_visibility(key0, T, n, m0, m1);
                 float mx = -INFINITY;
 #pragma unroll
-                for (int k = 0; k < 64; ++k) {
-                    const uint32_t bit = (k < 32 ? (vis_lo >> k) : (vis_hi >> (k - 32))) & 1u;
-                    s[k] = bit ? s[k] * a.scale_log2 : -INFINITY;
+                for (int k = 0; k < 32; ++k) {
+                    s[k] = ((vis >> k) & 1u) ? s[k] * a.scale_log2 : -INFINITY;
                     mx = fmaxf(mx, s[k]);
                 }
+                float mx_other;
+                if (!swap_with_other_half(jj, mx, mx_other)) {
+                    ok = false;
+                    break;
+                }
+                mx = fmaxf(mx, mx_other);
                 float alpha = 1.0f;  // rescale factor of this row's O for this tile
                 if (mx > m_ref + kRescaleThreshold) {
                     alpha = ex2_approx(m_ref - mx);  // 0 while nothing was visible before
@@ -573,14 +600,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // P = hi + lo, both bf16. While no key has been visible yet
                 // m_ref is -inf and every s is -inf: subtracting 0 keeps p = 0.
                 const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
-                uint32_t pk_hi[32], pk_lo[32];
+                uint32_t pw[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
+                for (int k = 0; k < 16; ++k) {
                     const float p0 = ex2_approx(s[2 * k] - mref);
                     const float p1 = ex2_approx(s[2 * k + 1] - mref);
                     const uint32_t h = pack_bf16x2(p0, p1);
-                    pk_hi[k] = h;
-                    pk_lo[k] = pack_bf16x2(p0 - bf16lo_to_f32(h), p1 - bf16hi_to_f32(h));
+                    pw[k] = h;
+                    pw[16 + k] = pack_bf16x2(p0 - bf16lo_to_f32(h), p1 - bf16hi_to_f32(h));
                     l_sum += p0 + p1;
                 }
                 // ship P and the rescale factor to the partner
@@ -589,24 +616,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
 #pragma unroll
-                for (int w4 = 0; w4 < 8; ++w4) {
-                    st_async_v4(r_px + (w4 * kOwnRows + lr) * 16,
-                                make_uint4(pk_hi[4 * w4], pk_hi[4 * w4 + 1], pk_hi[4 * w4 + 2], pk_hi[4 * w4 + 3]),
-                                r_bar_px_full);
-                    st_async_v4(r_px + ((w4 + 8) * kOwnRows + lr) * 16,
-                                make_uint4(pk_lo[4 * w4], pk_lo[4 * w4 + 1], pk_lo[4 * w4 + 2], pk_lo[4 * w4 + 3]),
-                                r_bar_px_full);
-                }
-                st_async_b32(r_ax + lr * 4, __float_as_uint(alpha), r_bar_px_full);
-                if (!publish(jj, alpha, pk_hi, pk_lo)) ok = false;
+                for (int i = 0; i < 8; ++i)
+                    st_async_v4(r_px + ((grp0 + i) * kOwnRows + lr) * 16,
+                                make_uint4(pw[4 * i], pw[4 * i + 1], pw[4 * i + 2], pw[4 * i + 3]), r_bar_px_full);
+                if (half == 0) st_async_b32(r_ax + lr * 4, __float_as_uint(alpha), r_bar_px_full);
+                if (!publish(jj, alpha, pw)) ok = false;
             }
+            // the row sum is the two halves' sums (same reference max)
+            float l_other;
+            if (ok && !swap_with_other_half(nt, l_sum, l_other)) ok = false;
+            if (ok) l_sum += l_other;
         } else {
             // ---- the partner's rows, one tile behind: ship tile jj's partial
             // S first, then take tile jj-1's probabilities, so the round trip
             // to the partner overlaps a whole tile
             for (int jj = 0; jj <= nt && ok; ++jj) {
                 if (jj < nt) {
-                    uint32_t sv[64];
+                    uint32_t sv[32];
                     if (!load_s(jj, sv)) {
                         ok = false;
                         break;
@@ -616,35 +642,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
 #pragma unroll
-                    for (int k4 = 0; k4 < 16; ++k4)
-                        st_async_v4(r_sx + (k4 * kOwnRows + lr) * 16,
-                                    make_uint4(sv[4 * k4], sv[4 * k4 + 1], sv[4 * k4 + 2], sv[4 * k4 + 3]),
+                    for (int i = 0; i < 8; ++i)
+                        st_async_v4(r_sx + ((grp0 + i) * kOwnRows + lr) * 16,
+                                    make_uint4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]),
                                     r_bar_sx_full);
                 }
                 if (jj >= 1) {
                     const int t = jj - 1;
                     // one helper thread arms the phase: 64 rows x 256 B of P + 64 factors
-                    if (lr == 0) mbar_arrive_expect_tx(bar(BAR_PX_FULL), kPXBytes + kOwnRows * 4);
+                    if (lead) mbar_arrive_expect_tx(bar(BAR_PX_FULL), kPXBytes + kOwnRows * 4);
                     if (!wwait_cluster(bar(BAR_PX_FULL), t & 1)) {
                         ok = false;
                         break;
                     }
-                    uint32_t pk_hi[32], pk_lo[32];
+                    uint32_t pw[32];
 #pragma unroll
-                    for (int w4 = 0; w4 < 8; ++w4) {
-                        const uint4 h = px[w4 * kOwnRows + lr];
-                        const uint4 l = px[(w4 + 8) * kOwnRows + lr];
-                        pk_hi[4 * w4] = h.x;
-                        pk_hi[4 * w4 + 1] = h.y;
-                        pk_hi[4 * w4 + 2] = h.z;
-                        pk_hi[4 * w4 + 3] = h.w;
-                        pk_lo[4 * w4] = l.x;
-                        pk_lo[4 * w4 + 1] = l.y;
-                        pk_lo[4 * w4 + 2] = l.z;
-                        pk_lo[4 * w4 + 3] = l.w;
+                    for (int i = 0; i < 8; ++i) {
+                        const uint4 w = px[(grp0 + i) * kOwnRows + lr];
+                        pw[4 * i] = w.x;
+                        pw[4 * i + 1] = w.y;
+                        pw[4 * i + 2] = w.z;
+                        pw[4 * i + 3] = w.w;
                     }
                     const float alpha = ax[lr];
-                    if (!publish(t, alpha, pk_hi, pk_lo)) ok = false;
+                    if (!publish(t, alpha, pw)) ok = false;
                     // the values read from PX are in tensor memory now
                     // (publish waited for its tcgen05.st), so the buffer can
                     // be handed back without a release, which would also wait
@@ -655,9 +676,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (ok && !wwait(bar(BAR_O_FINAL), 0)) ok = false;
         // final row sums: owners hand theirs to the partner's other half
-        if (ok && owner) st_async_b32(r_lx + lr * 4, __float_as_uint(l_sum), r_bar_lx_full);
+        if (ok && owner && half == 0) st_async_b32(r_lx + lr * 4, __float_as_uint(l_sum), r_bar_lx_full);
         if (ok && !owner) {
-            if (lr == 0) mbar_arrive_expect_tx(bar(BAR_LX_FULL), kOwnRows * 4);
+            if (lead) mbar_arrive_expect_tx(bar(BAR_LX_FULL), kOwnRows * 4);
             if (!wwait_cluster(bar(BAR_LX_FULL), 0)) ok = false;
             else l_sum = lx[lr];
         }
@@ -667,11 +688,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             tc_fence_after();
             const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-            float *dst = o_dst + (row_base + g) * 512 + rank * 256;
+            float *dst = o_dst + (row_base + g) * 512 + rank * 256 + half * 128;
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_base + kColO + c * 32, o);
+                tmem_ld32(tmem + lane_base + kColO + half * 128 + c * 32, o);
                 tmem_wait_ld();
                 if (row_in_seq) {
                     float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
@@ -682,7 +703,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                             __uint_as_float(o[4 * v + 3]) * inv_l);
                 }
             }
-            if (owner && row_in_seq)
+            if (owner && half == 0 && row_in_seq)
                 lse_dst[row_base + g] = l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
         }
     }
@@ -690,7 +711,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     // neither CTA may leave while its partner can still write into it
     cluster_sync();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
