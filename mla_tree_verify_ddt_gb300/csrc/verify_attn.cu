@@ -66,7 +66,6 @@ namespace ddt {
 namespace {
 
 constexpr int kRows = 128;          // rows per cluster (MMA M)
-constexpr int kOwnRows = 64;        // rows whose softmax one CTA runs
 constexpr int kKeys = 64;           // keys per tile (S MMA N)
 constexpr int kQChunks = 4;         // latent query/KV chunks per CTA: 4 x 64 columns
 constexpr int kQSmemChunks = 3;     // query chunks 0-2 in shared memory; chunk 3 and the
@@ -81,15 +80,10 @@ constexpr int kSPBufs = 3;          // S / P buffers in tensor memory
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kOffQ + kQSmemChunks * kChunkBytesQ;     // 49152
-constexpr int kOffSX = kOffRing + kSlots * kSlotBytes;            // 196608: partner's partial S, my rows
-constexpr int kSXBytes = kOwnRows * kKeys * 4;                    // 16384
-constexpr int kOffPX = kOffSX + kSXBytes;                         // 212992: partner's P (hi, lo) for my other rows
-constexpr int kPXBytes = kOwnRows * kKeys * 4;                    // 16384 (32 hi + 32 lo words per row)
-constexpr int kOffAX = kOffPX + kPXBytes;                         // 229376: rescale factor per row
-constexpr int kOffLX = kOffAX + kOwnRows * 4;                     // 229632: final row sum per row
-constexpr int kOffBar = kOffLX + kOwnRows * 4;                    // 229888: barriers and flags (256 B)
-constexpr int kOffMX = kOffBar + 256;                             // 230144: [2 rounds][2 key halves][64 rows]
-constexpr int kSmemBytes = kOffMX + 2 * 2 * kOwnRows * 4 + 1024;  // + alignment slack
+constexpr int kOffSX = kOffRing + kSlots * kSlotBytes;            // 196608: the partner's partial S of a tile
+constexpr int kSXBytes = kRows * kKeys * 4;                       // 32768
+constexpr int kOffBar = kOffSX + kSXBytes;                        // 229376: barriers and flags (256 B)
+constexpr int kSmemBytes = kOffBar + 256 + 1024;                  // + alignment slack
 
 // tensor memory columns
 constexpr uint32_t kColO = 0;       // 256: this CTA's half of O
@@ -97,6 +91,7 @@ constexpr uint32_t kColSP = 256;    // 3 x 64: partial S of a tile, overwritten 
                                     // lane, once read) by its P: 32 hi words then 32 lo words
 constexpr uint32_t kColQ3 = 448;    // 32: latent query chunk 3 (bf16 pairs)
 constexpr uint32_t kColQR = 480;    // 16: rotary query (bf16 pairs)
+constexpr uint32_t kColX = 496;     // 4: [round parity][key half] word the two threads of a row swap
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -115,15 +110,12 @@ enum {
     BAR_O_FINAL = 19,
     BAR_DRAIN = 20,
     // exchange barriers, arrived on by the partner CTA's threads
-    BAR_SX_FULL = 21,    // partner wrote its partial S rows into my SX
-    BAR_SX_EMPTY = 22,   // partner read the partial S rows I wrote into its SX
-    BAR_PX_FULL = 23,    // partner wrote P for my other rows into my PX
-    BAR_PX_EMPTY = 24,   // partner read the P I wrote into its PX
-    BAR_LX_FULL = 25,    // partner wrote final row sums into my LX
-    // the two threads of an owned row swap their halves' tile max (and, at
-    // the end, their row sums): one barrier per owned TMEM quadrant
-    BAR_MAXX = 26,       // 2
-    NUM_BARS = 28
+    BAR_SX_FULL = 21,    // partner's partial S of the tile is in my SX
+    BAR_SX_EMPTY = 22,   // partner has read the partial S I wrote into its SX
+    // the two threads of a row swap their halves' tile max (and, at the end,
+    // their row sums): one barrier per TMEM lane quadrant
+    BAR_MAXX = 23,       // 4
+    NUM_BARS = 27
 };
 
 struct AttnArgs {
@@ -229,15 +221,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(BAR_O_FINAL), 1);
         mbar_init(bar(BAR_DRAIN), 1);
-        // the FULL barriers complete on bytes: one local thread arms each
-        // phase with expect_tx and the partner's st.async credits the bytes
+        // SX_FULL completes on bytes: one local thread arms each phase with
+        // expect_tx and the partner's st.async credits the bytes
         mbar_init(bar(BAR_SX_FULL), 1);
-        mbar_init(bar(BAR_SX_EMPTY), 2 * kOwnRows);
-        mbar_init(bar(BAR_PX_FULL), 1);
-        mbar_init(bar(BAR_PX_EMPTY), 2 * kOwnRows);
-        mbar_init(bar(BAR_MAXX), 64);
-        mbar_init(bar(BAR_MAXX + 1), 64);
-        mbar_init(bar(BAR_LX_FULL), 1);
+        mbar_init(bar(BAR_SX_EMPTY), 2 * kRows);
+        for (int q = 0; q < 4; ++q) mbar_init(bar(BAR_MAXX + q), 2);  // warps q and q+4
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -407,42 +395,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // ======================= softmax group (warps 0-7) =======================
         // Warp w serves tensor-memory lanes 32(w%4)..+31 (one row per lane)
-        // and key half c = w/4 of every tile: keys [32c, 32c+32). The two
-        // threads of a row agree on the row max through shared memory once
-        // per tile and add their row sums at the end.
+        // and key half c = w/4 of every tile: keys [32c, 32c+32). Per tile a
+        // thread ships its partial S to the partner, adds the partner's
+        // partial to its own, and runs the softmax of its row and key half.
+        // Both CTAs then hold the same full S and compute the same P (fp32
+        // addition commutes), each for its own half of O. The two threads of
+        // a row agree on the row max through shared memory.
         const int quad = warp & 3, half = warp >> 2;
         const int row = quad * 32 + lane;            // TMEM lane of this thread
-        const bool owner = (row >> 6) == static_cast<int>(rank);
-        const int lr = row & (kOwnRows - 1);         // row index within its 64-row half
         const int g = mt * kRows + row;              // row within the sequence
         const bool row_in_seq = g < rows_seq;
         const int node = g / a.H;
         const bool node_ok = row_in_seq && node < n && seq_ok;
-        const bool lead = lr == 0 && half == 0;      // arms the exchange barriers' byte counts
+        const bool lead = row == 0 && half == 0;     // arms each tile's SX byte count
         uint64_t m0 = 0, m1 = 0;
-        if (owner && node_ok) {
+        if (node_ok) {
             const uint64_t *mk = a.mask + (static_cast<size_t>(b) * a.Qc + node) * a.W;
             m0 = mk[0];
             if (a.W > 1) m1 = mk[1];
         }
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t col_half = static_cast<uint32_t>(half) * 32;   // this thread's 32 columns of an S/P buffer
-        const uint4 *sx = reinterpret_cast<const uint4 *>(smem + kOffSX);   // [16][64 rows] of 4 floats
-        const uint4 *px = reinterpret_cast<const uint4 *>(smem + kOffPX);   // [16][64 rows] of 4 words
-        const volatile float *ax = reinterpret_cast<const volatile float *>(smem + kOffAX);
-        const volatile float *lx = reinterpret_cast<const volatile float *>(smem + kOffLX);
-        volatile float *mx_x = reinterpret_cast<volatile float *>(smem + kOffMX);  // [2][2][64]
-        // the partner's copies of the exchange buffers and barriers
+        const uint4 *sx = reinterpret_cast<const uint4 *>(smem + kOffSX);   // [16 groups][128 rows] of 4 floats
         const uint32_t r_sx = mapa_shared(sbase + kOffSX, peer);
-        const uint32_t r_px = mapa_shared(sbase + kOffPX, peer);
-        const uint32_t r_ax = mapa_shared(sbase + kOffAX, peer);
-        const uint32_t r_lx = mapa_shared(sbase + kOffLX, peer);
         const uint32_t r_bar_sx_full = mapa_shared(bar(BAR_SX_FULL), peer);
         const uint32_t r_bar_sx_empty = mapa_shared(bar(BAR_SX_EMPTY), peer);
-        const uint32_t r_bar_px_full = mapa_shared(bar(BAR_PX_FULL), peer);
-        const uint32_t r_bar_px_empty = mapa_shared(bar(BAR_PX_EMPTY), peer);
-        const uint32_t r_bar_lx_full = mapa_shared(bar(BAR_LX_FULL), peer);
-        // SX / PX hold a row's 64 words as 16 groups of 4; this half's are groups 8c..8c+7
+        // a row's 64 partial scores are 16 groups of 4; this half's are groups 8c..8c+7
         const int grp0 = half * 8;
 
         // waits of the softmax group are made warp-uniform, so a lane that
@@ -453,13 +431,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto wwait_cluster = [&](uint32_t barrier, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait_cluster(barrier, parity, deadline, abort_flag));
         };
-        // The two threads of an owned row swap one float through shared
-        // memory: round k uses buffer k&1 and phase k of the quadrant's barrier.
+        // The two threads of a row (same tensor-memory lane, warps q and
+        // q+4) swap one float through a tensor-memory word: round k uses the
+        // words of parity k&1 and phase k of the quadrant's barrier.
         auto swap_with_other_half = [&](int k, float v, float &other) -> bool {
-            mx_x[((k & 1) * 2 + half) * kOwnRows + lr] = v;
-            mbar_arrive(bar(BAR_MAXX + (quad & 1)));
-            if (!wwait(bar(BAR_MAXX + (quad & 1)), k & 1)) return false;
-            other = mx_x[((k & 1) * 2 + (half ^ 1)) * kOwnRows + lr];
+            tmem_st1(tmem + lane_base + kColX + (k & 1) * 2 + half, __float_as_uint(v));
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_MAXX + quad));
+            if (!wwait(bar(BAR_MAXX + quad), k & 1)) return false;
+            __syncwarp();
+            tc_fence_after();
+            other = __uint_as_float(tmem_ld1(tmem + lane_base + kColX + (k & 1) * 2 + (half ^ 1)));
+            tmem_wait_ld();
             return true;
         };
 
@@ -493,8 +478,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(BAR_QT_READY));
         }
 
-        // this thread's 32 keys of the partial S of tile t, from tensor memory
-        auto load_s = [&](int t, uint32_t (&sv)[32]) -> bool {
+        // this CTA's partial S of tile t, this thread's 32 keys
+        auto load_own = [&](int t, uint32_t (&sv)[32]) -> bool {
             const int sb = t % kSPBufs;
             if (!wwait(bar(BAR_S_FULL + sb), (t / kSPBufs) & 1)) return false;
             __syncwarp();
@@ -503,14 +488,95 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             return true;
         };
-        // P of tile t for this thread's 32 keys (16 hi words, then 16 lo
-        // words) into this CTA's tensor memory, over the thread's own (already
-        // read) S columns, after the row's O half has been rescaled by alpha;
-        // the rescale needs O quiescent (PV of t-1 done)
-        auto publish = [&](int t, float alpha, const uint32_t (&pw)[32]) -> bool {
-            const int pb = t % kSPBufs;
-            if (__any_sync(0xffffffffu, alpha != 1.0f) && t >= 1) {
-                if (!wwait(bar(BAR_PV_DONE + ((t - 1) % kSPBufs)), ((t - 1) / kSPBufs) & 1)) return false;
+        auto ship = [&](const uint32_t (&sv)[32]) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                st_async_v4(r_sx + ((grp0 + i) * kRows + row) * 16,
+                            make_uint4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]), r_bar_sx_full);
+        };
+
+        float m_ref = -INFINITY, l_sum = 0.f;
+        bool ok = true;
+        // The partial of tile t+1 is loaded and shipped before the softmax of
+        // tile t, so its transfer to the partner overlaps that softmax.
+        uint32_t sv[32];
+        if (!load_own(0, sv)) ok = false;
+        else ship(sv);
+        for (int jj = 0; jj < nt && ok; ++jj) {
+            const int sb = jj % kSPBufs;
+            const int key0 = (t0 + jj) * kKeys + half * 32;
+            // ---- the partner's partial of tile jj: 128 rows x 256 B
+            if (lead) mbar_arrive_expect_tx(bar(BAR_SX_FULL), kSXBytes);
+            if (!wwait_cluster(bar(BAR_SX_FULL), jj & 1)) {
+                ok = false;
+                break;
+            }
+            float s[32];
+            uint32_t read_dep = 0;  // depends on every word read from SX
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint4 o = sx[(grp0 + i) * kRows + row];
+                read_dep ^= o.x ^ o.y ^ o.z ^ o.w;
+                s[4 * i] = __uint_as_float(sv[4 * i]) + __uint_as_float(o.x);
+                s[4 * i + 1] = __uint_as_float(sv[4 * i + 1]) + __uint_as_float(o.y);
+                s[4 * i + 2] = __uint_as_float(sv[4 * i + 2]) + __uint_as_float(o.z);
+                s[4 * i + 3] = __uint_as_float(sv[4 * i + 3]) + __uint_as_float(o.w);
+            }
+            // hand the buffer back once every read of it is done (the arrive
+            // waits for read_dep); a release would also wait for this
+            // thread's st.async to land in the partner
+            mbar_arrive_remote_relaxed_after(r_bar_sx_empty, read_dep, sBar + NUM_BARS * 8 + 8);
+            // ---- next tile's partial: load it, and ship it once the partner
+            // has read this tile's
+            if (jj + 1 < nt) {
+                if (!load_own(jj + 1, sv) || !wwait_cluster(bar(BAR_SX_EMPTY), jj & 1)) {
+                    ok = false;
+                    break;
+                }
+                ship(sv);
+            }
+            // ---- masked online softmax, log2 domain
+            uint32_t vis = ~0u;
+            if (!node_ok) vis = 0;
+            else if (key0 + 32 > T) vis = half_tile_visibility(key0, T, n, m0, m1);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                s[k] = ((vis >> k) & 1u) ? s[k] * a.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[k]);
+            }
+            float mx_other;
+            if (!swap_with_other_half(jj, mx, mx_other)) {
+                ok = false;
+                break;
+            }
+            mx = fmaxf(mx, mx_other);
+            float alpha = 1.0f;  // rescale factor of this row's O for this tile
+            if (mx > m_ref + kRescaleThreshold) {
+                alpha = ex2_approx(m_ref - mx);  // 0 while nothing was visible before
+                m_ref = mx;
+                l_sum *= alpha;
+            }
+            // P = hi + lo, both bf16. While no key has been visible yet
+            // m_ref is -inf and every s is -inf: subtracting 0 keeps p = 0.
+            const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
+            uint32_t pw[32];  // 16 hi words, then 16 lo words
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float p0 = ex2_approx(s[2 * k] - mref);
+                const float p1 = ex2_approx(s[2 * k + 1] - mref);
+                const uint32_t h = pack_bf16x2(p0, p1);
+                pw[k] = h;
+                pw[16 + k] = pack_bf16x2(p0 - bf16lo_to_f32(h), p1 - bf16hi_to_f32(h));
+                l_sum += p0 + p1;
+            }
+            // ---- rescale this thread's half of the row's O (needs PV of the
+            // previous tile done), then publish P over the S it replaces
+            if (__any_sync(0xffffffffu, alpha != 1.0f) && jj >= 1) {
+                if (!wwait(bar(BAR_PV_DONE + ((jj - 1) % kSPBufs)), ((jj - 1) / kSPBufs) & 1)) {
+                    ok = false;
+                    break;
+                }
                 __syncwarp();
                 tc_fence_after();
 #pragma unroll 1
@@ -527,161 +593,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // KV rows past the last node may hold anything (NaN included) and
             // P is 0 there, but 0 * NaN is NaN: zero those V rows of the tail
             // tile (S, which read them as K, is already complete)
-            const int key0 = (t0 + t) * kKeys;
-            if (key0 + kKeys > kend) {
-                uint4 *vset = reinterpret_cast<uint4 *>(smem + kOffRing + (t % kSlots) * kSlotBytes);
-                const int kvalid = kend - key0;
+            if ((t0 + jj) * kKeys + kKeys > kend) {
+                uint4 *vset = reinterpret_cast<uint4 *>(smem + kOffRing + (jj % kSlots) * kSlotBytes);
+                const int kvalid = kend - (t0 + jj) * kKeys;
 #pragma unroll 1
                 for (int e = half * kRows + row; e < kQChunks * kChunkBytesKV / 16; e += 2 * kRows)
                     if (((e >> 3) & (kKeys - 1)) >= kvalid) vset[e] = make_uint4(0, 0, 0, 0);
                 fence_proxy_async_smem();
             }
-            tmem_st32(tmem + lane_base + kColSP + pb * 64 + col_half, pw);
+            tmem_st32(tmem + lane_base + kColSP + sb * 64 + col_half, pw);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_P_FULL + pb));
-            return true;
-        };
-
-        float m_ref = -INFINITY, l_sum = 0.f;
-        bool ok = true;
-        if (owner) {
-            // ---- own rows: add the partner's partial, softmax, ship P back
-            for (int jj = 0; jj < nt && ok; ++jj) {
-                const int key0 = (t0 + jj) * kKeys + half * 32;
-                uint32_t sv[32];
-                if (!load_s(jj, sv)) {
-                    ok = false;
-                    break;
-                }
-                // one owner thread arms this tile's phase: 64 rows x 256 B
-                if (lead) mbar_arrive_expect_tx(bar(BAR_SX_FULL), kSXBytes);
-                if (!wwait_cluster(bar(BAR_SX_FULL), jj & 1)) {
-                    ok = false;
-                    break;
-                }
-                float s[32];
-                uint32_t read_dep = 0;  // depends on every word read from SX
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint4 o = sx[(grp0 + i) * kOwnRows + lr];
-                    read_dep ^= o.x ^ o.y ^ o.z ^ o.w;
-                    s[4 * i] = __uint_as_float(sv[4 * i]) + __uint_as_float(o.x);
-                    s[4 * i + 1] = __uint_as_float(sv[4 * i + 1]) + __uint_as_float(o.y);
-                    s[4 * i + 2] = __uint_as_float(sv[4 * i + 2]) + __uint_as_float(o.z);
-                    s[4 * i + 3] = __uint_as_float(sv[4 * i + 3]) + __uint_as_float(o.w);
-                }
-                // hand the partner's buffer back once every read of it is done
-                // (the arrive waits for read_dep); a release would also wait
-                // for this thread's st.async of the previous tile's P
-                mbar_arrive_remote_relaxed_after(r_bar_sx_empty, read_dep, sBar + NUM_BARS * 8 + 8);
-                uint32_t vis = ~0u;
-                if (!node_ok) vis = 0;
-                else if (key0 + 32 > T) vis = half_tile_visibility(key0, T, n, m0, m1);
-                float mx = -INFINITY;
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    s[k] = ((vis >> k) & 1u) ? s[k] * a.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, s[k]);
-                }
-                float mx_other;
-                if (!swap_with_other_half(jj, mx, mx_other)) {
-                    ok = false;
-                    break;
-                }
-                mx = fmaxf(mx, mx_other);
-                float alpha = 1.0f;  // rescale factor of this row's O for this tile
-                if (mx > m_ref + kRescaleThreshold) {
-                    alpha = ex2_approx(m_ref - mx);  // 0 while nothing was visible before
-                    m_ref = mx;
-                    l_sum *= alpha;
-                }
-                // P = hi + lo, both bf16. While no key has been visible yet
-                // m_ref is -inf and every s is -inf: subtracting 0 keeps p = 0.
-                const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
-                uint32_t pw[32];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float p0 = ex2_approx(s[2 * k] - mref);
-                    const float p1 = ex2_approx(s[2 * k + 1] - mref);
-                    const uint32_t h = pack_bf16x2(p0, p1);
-                    pw[k] = h;
-                    pw[16 + k] = pack_bf16x2(p0 - bf16lo_to_f32(h), p1 - bf16hi_to_f32(h));
-                    l_sum += p0 + p1;
-                }
-                // ship P and the rescale factor to the partner
-                if (jj >= 1 && !wwait_cluster(bar(BAR_PX_EMPTY), (jj - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    st_async_v4(r_px + ((grp0 + i) * kOwnRows + lr) * 16,
-                                make_uint4(pw[4 * i], pw[4 * i + 1], pw[4 * i + 2], pw[4 * i + 3]), r_bar_px_full);
-                if (half == 0) st_async_b32(r_ax + lr * 4, __float_as_uint(alpha), r_bar_px_full);
-                if (!publish(jj, alpha, pw)) ok = false;
-            }
-            // the row sum is the two halves' sums (same reference max)
-            float l_other;
-            if (ok && !swap_with_other_half(nt, l_sum, l_other)) ok = false;
-            if (ok) l_sum += l_other;
-        } else {
-            // ---- the partner's rows, one tile behind: ship tile jj's partial
-            // S first, then take tile jj-1's probabilities, so the round trip
-            // to the partner overlaps a whole tile
-            for (int jj = 0; jj <= nt && ok; ++jj) {
-                if (jj < nt) {
-                    uint32_t sv[32];
-                    if (!load_s(jj, sv)) {
-                        ok = false;
-                        break;
-                    }
-                    if (jj >= 1 && !wwait_cluster(bar(BAR_SX_EMPTY), (jj - 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        st_async_v4(r_sx + ((grp0 + i) * kOwnRows + lr) * 16,
-                                    make_uint4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]),
-                                    r_bar_sx_full);
-                }
-                if (jj >= 1) {
-                    const int t = jj - 1;
-                    // one helper thread arms the phase: 64 rows x 256 B of P + 64 factors
-                    if (lead) mbar_arrive_expect_tx(bar(BAR_PX_FULL), kPXBytes + kOwnRows * 4);
-                    if (!wwait_cluster(bar(BAR_PX_FULL), t & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    uint32_t pw[32];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint4 w = px[(grp0 + i) * kOwnRows + lr];
-                        pw[4 * i] = w.x;
-                        pw[4 * i + 1] = w.y;
-                        pw[4 * i + 2] = w.z;
-                        pw[4 * i + 3] = w.w;
-                    }
-                    const float alpha = ax[lr];
-                    if (!publish(t, alpha, pw)) ok = false;
-                    // the values read from PX are in tensor memory now
-                    // (publish waited for its tcgen05.st), so the buffer can
-                    // be handed back without a release, which would also wait
-                    // for this thread's st.async of tile jj
-                    mbar_arrive_remote_relaxed(r_bar_px_empty);
-                }
-            }
+            if (lane == 0) mbar_arrive(bar(BAR_P_FULL + sb));
         }
+        // the row sum is the two halves' sums (same reference max)
+        float l_other;
+        if (ok && !swap_with_other_half(nt, l_sum, l_other)) ok = false;
+        if (ok) l_sum += l_other;
         if (ok && !wwait(bar(BAR_O_FINAL), 0)) ok = false;
-        // final row sums: owners hand theirs to the partner's other half
-        if (ok && owner && half == 0) st_async_b32(r_lx + lr * 4, __float_as_uint(l_sum), r_bar_lx_full);
-        if (ok && !owner) {
-            if (lead) mbar_arrive_expect_tx(bar(BAR_LX_FULL), kOwnRows * 4);
-            if (!wwait_cluster(bar(BAR_LX_FULL), 0)) ok = false;
-            else l_sum = lx[lr];
-        }
         if (!ok) {
             fail();
         } else {
@@ -703,7 +633,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                             __uint_as_float(o[4 * v + 3]) * inv_l);
                 }
             }
-            if (owner && half == 0 && row_in_seq)
+            // both CTAs hold the same row sum and max; one writes the lse
+            if (rank == 0 && half == 0 && row_in_seq)
                 lse_dst[row_base + g] = l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
         }
     }
