@@ -527,14 +527,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // thread's st.async to land in the partner
             mbar_arrive_remote_relaxed_after(r_bar_sx_empty, read_dep, sBar + NUM_BARS * 8 + 8);
             // ---- next tile's partial: load it, and ship it once the partner
-            // has read this tile's
-            if (jj + 1 < nt) {
-                if (!load_own(jj + 1, sv) || !wwait_cluster(bar(BAR_SX_EMPTY), jj & 1)) {
-                    ok = false;
-                    break;
-                }
-                ship(sv);
+            // has read this tile's. The eight stores are spread over the
+            // softmax below: the link to the partner drains at a few tens of
+            // GB/s, and a burst of them would stall this thread until it has.
+            const bool ship_next = jj + 1 < nt;
+            if (ship_next && (!load_own(jj + 1, sv) || !wwait_cluster(bar(BAR_SX_EMPTY), jj & 1))) {
+                ok = false;
+                break;
             }
+            auto ship_group = [&](int i) {
+                if (ship_next)
+                    st_async_v4(r_sx + ((grp0 + i) * kRows + row) * 16,
+                                make_uint4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]), r_bar_sx_full);
+            };
             // ---- masked online softmax, log2 domain
             uint32_t vis = ~0u;
             if (!node_ok) vis = 0;
@@ -542,6 +547,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float mx = -INFINITY;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
+                if ((k & 7) == 0) ship_group(k >> 3);
                 s[k] = ((vis >> k) & 1u) ? s[k] * a.scale_log2 : -INFINITY;
                 mx = fmaxf(mx, s[k]);
             }
@@ -563,6 +569,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t pw[32];  // 16 hi words, then 16 lo words
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
+                if ((k & 3) == 0) ship_group(4 + (k >> 2));
                 const float p0 = ex2_approx(s[2 * k] - mref);
                 const float p1 = ex2_approx(s[2 * k + 1] - mref);
                 const uint32_t h = pack_bf16x2(p0, p1);
