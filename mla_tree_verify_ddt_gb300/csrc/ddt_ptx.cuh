@@ -160,6 +160,17 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed_after(uint32_t remote
         : "memory");
 }
 
+// Split whole-cluster barrier. An arriving thread with release semantics
+// first waits for all of its earlier memory operations (global loads
+// included) to be performed; a relaxed arrival orders nothing.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
 // Whole-cluster barrier (every thread of every CTA of the cluster).
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -187,6 +198,23 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int c0,
                      reinterpret_cast<uint64_t>(m)),
                  "r"(c0), "r"(c1)
                  : "memory");
+}
+
+// 3D tile store shared -> global, tracked by this thread's bulk async-group.
+// Elements outside the tensor's bounds are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until every bulk async-group of this thread has finished reading its
+// shared-memory source (the global writes complete with the grid).
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -33,24 +33,32 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     int n = n_nodes[b];
     n = n < 1 ? 1 : (n > Qc ? Qc : n);
     // each lane caches the (parent, token) of nodes lane+1, lane+33, lane+65
-    int par[3], tok[3];
+    // and the target's argmax after nodes lane, lane+32, lane+64, so the walk
+    // below never waits on global memory
+    int par[3], tok[3], tgt[3];
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
         const int j = lane + 1 + 32 * k;
         par[k] = (j < n) ? parent[tb + j] : -2;
         tok[k] = (j < n) ? token[tb + j] : 0;
+        const int c = lane + 32 * k;
+        tgt[k] = (c < n) ? target[tb + c] : 0;
     }
+    // the target's argmax after node c (c < n)
+    auto target_after = [&](int c) {
+        const int v = (c >> 5) == 0 ? tgt[0] : ((c >> 5) == 1 ? tgt[1] : tgt[2]);
+        return __shfl_sync(0xffffffffu, v, c & 31);
+    };
     int32_t *ai = accept_idx + static_cast<size_t>(b) * (D + 1);
     int32_t *ct = commit_tok + static_cast<size_t>(b) * (D + 1);
     int cur = 0, len = 1;
-    int t = target[tb];
+    int t = target_after(0);
     for (;;) {
         int found = 0x7fffffff;
 #pragma unroll
         for (int k = 0; k < 3; ++k)
             if (par[k] == cur && tok[k] == t) found = min(found, lane + 1 + 32 * k);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) found = min(found, __shfl_xor_sync(0xffffffffu, found, off));
+        found = static_cast<int>(__reduce_min_sync(0xffffffffu, static_cast<unsigned>(found)));
         if (found == 0x7fffffff || len > D) break;
         if (lane == 0) {
             ct[len - 1] = t;  // the accepted child's token equals t
@@ -58,7 +66,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
         }
         ++len;
         cur = found;
-        t = target[tb + cur];
+        t = target_after(cur);
     }
     for (int k = lane; k <= D; k += 32) {
         if (k == 0) ai[0] = 0;

@@ -13,9 +13,11 @@
 // which the frontier realises exactly: a node's first child and next sibling
 // both come after it in that order, so popping the frontier minimum each step
 // yields the global order. The frontier never holds more than budget+1
-// entries; each lane owns three slots and the warp finds the minimum with
-// shuffles. The rank path is packed into 64 bits, four per level, level 1 in
-// the top nibble, so two paths of equal depth compare as integers.
+// entries. It lives in registers, three slots per lane; a pop is one warp
+// min-reduction of the 32-bit score key (redux.sync), with depth and rank
+// path consulted only when scores tie. The rank path is packed into 64 bits,
+// four per level, level 1 in the top nibble, so two paths of equal depth
+// compare as integers.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -30,22 +32,32 @@ constexpr int kFrontierSlots = 3;  // per lane: 96 >= budget + 1
 constexpr int kWarpsPerBlock = 4;
 constexpr int kMaxQc = DDT_MAX_BUDGET + 1;
 constexpr int kMaxDK = DDT_MAX_DEPTH * DDT_MAX_TOPK;
+constexpr uint32_t kNoKey = 0xffffffffu;  // above every score key, -inf included
+constexpr unsigned kAll = 0xffffffffu;
 
-// Sort key: smaller is selected first.
-struct Key {
-    uint64_t hi;  // inverted ordered score (32) | depth (32)
-    uint64_t lo;  // rank path
-};
-
-__device__ __forceinline__ uint32_t ordered_desc(float s) {
-    s = s + 0.0f;  // -0 -> +0 so equal scores share one key
-    uint32_t u = __float_as_uint(s);
-    uint32_t asc = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return ~asc;  // larger score -> smaller key
+// Order-preserving map of a score to a key where the larger score gets the
+// smaller key (-0 and +0 share one key).
+__device__ __forceinline__ uint32_t score_key(float s) {
+    s = s + 0.0f;
+    const uint32_t u = __float_as_uint(s);
+    const uint32_t asc = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ~asc;
 }
 
-__device__ __forceinline__ bool key_less(const Key &a, const Key &b) {
-    return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+// One frontier slot. Unused slots have key == kNoKey.
+struct Slot {
+    uint32_t key;     // score_key(score)
+    float score;
+    float pscore;     // the parent's score (for the next sibling's score)
+    int depth;
+    int parent;       // node index of the parent
+    uint64_t path;
+};
+
+__device__ __forceinline__ bool slot_less(const Slot &a, const Slot &b) {
+    if (a.key != b.key) return a.key < b.key;
+    if (a.depth != b.depth) return a.depth < b.depth;
+    return a.path < b.path;
 }
 
 struct WarpSmem {
@@ -53,13 +65,7 @@ struct WarpSmem {
     // one dependent chain, never wait on global memory
     float d_lp[kMaxDK];
     int d_tok[kMaxDK];
-    // frontier, slot = lane * kFrontierSlots + k
-    float f_score[32 * kFrontierSlots];
-    uint64_t f_path[32 * kFrontierSlots];
-    int f_depth[32 * kFrontierSlots];
-    int f_parent[32 * kFrontierSlots];
-    int f_valid[32 * kFrontierSlots];
-    // nodes
+    // nodes in pop order
     float n_score[kMaxQc];
     int n_parent[kMaxQc];
     int n_depth[kMaxQc];
@@ -101,9 +107,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     __syncwarp();
     for (int e = lane; e < D * K; e += 32)
         if ((e % K) > 0 && sm.d_lp[e] > sm.d_lp[e - 1]) bad = true;
-    bad = __any_sync(0xffffffffu, bad);
+    bad = __any_sync(kAll, bad);
 
-    for (int k = 0; k < kFrontierSlots; ++k) sm.f_valid[lane * kFrontierSlots + k] = 0;
     if (lane == 0) {
         sm.n_score[0] = 0.0f;
         sm.n_parent[0] = -1;
@@ -112,90 +117,102 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
         sm.n_token[0] = root;
         sm.n_mask[0][0] = 1ull;
         sm.n_mask[0][1] = 0ull;
+    }
+    Slot f[kFrontierSlots];
+#pragma unroll
+    for (int k = 0; k < kFrontierSlots; ++k) f[k] = Slot{kNoKey, 0.0f, 0.0f, 0, 0, 0ull};
+    if (lane == 0) {
         // the only initial candidate: depth 1, rank 0
-        sm.f_valid[0] = 1;
-        sm.f_score[0] = __fadd_rn(0.0f, sm.d_lp[0]);
-        sm.f_path[0] = 0ull;
-        sm.f_depth[0] = 1;
-        sm.f_parent[0] = 0;
+        const float s0 = __fadd_rn(0.0f, sm.d_lp[0]);
+        f[0] = Slot{score_key(s0), s0, 0.0f, 1, 0, 0ull};
     }
     __syncwarp();
 
     int n = 1;
     if (!bad) {
         while (n < budget + 1) {
-            // warp arg-min over the frontier
-            Key best{~0ull, ~0ull};
-            int best_slot = -1;
-            for (int k = 0; k < kFrontierSlots; ++k) {
-                const int slot = lane * kFrontierSlots + k;
-                if (!sm.f_valid[slot]) continue;
-                Key c{(static_cast<uint64_t>(ordered_desc(sm.f_score[slot])) << 32) |
-                          static_cast<uint32_t>(sm.f_depth[slot]),
-                      sm.f_path[slot]};
-                if (best_slot < 0 || key_less(c, best)) {
-                    best = c;
-                    best_slot = slot;
+            // ---- this lane's best slot
+            int ls = 0;
+            Slot mine = f[0];
+#pragma unroll
+            for (int k = 1; k < kFrontierSlots; ++k)
+                if (slot_less(f[k], mine)) {
+                    mine = f[k];
+                    ls = k;
+                }
+            // ---- the warp's best: score key first, depth and path on ties
+            const uint32_t mkey = __reduce_min_sync(kAll, mine.key);
+            if (mkey == kNoKey) break;  // frontier empty
+            if (mkey == score_key(-INFINITY)) break;  // everything left is -inf
+            unsigned tied = __ballot_sync(kAll, mine.key == mkey);
+            if (__popc(tied) > 1) {
+                const bool in1 = mine.key == mkey;
+                const uint32_t md = __reduce_min_sync(kAll, in1 ? static_cast<uint32_t>(mine.depth) : kNoKey);
+                const bool in2 = in1 && static_cast<uint32_t>(mine.depth) == md;
+                tied = __ballot_sync(kAll, in2);
+                if (__popc(tied) > 1) {
+                    const uint32_t ph = static_cast<uint32_t>(mine.path >> 32);
+                    const uint32_t mh = __reduce_min_sync(kAll, in2 ? ph : kNoKey);
+                    const bool in3 = in2 && ph == mh;
+                    tied = __ballot_sync(kAll, in3);
+                    if (__popc(tied) > 1) {
+                        const uint32_t pl = static_cast<uint32_t>(mine.path);
+                        const uint32_t ml = __reduce_min_sync(kAll, in3 ? pl : kNoKey);
+                        tied = __ballot_sync(kAll, in3 && pl == ml);  // paths are unique
+                    }
                 }
             }
-            for (int off = 16; off > 0; off >>= 1) {
-                Key o{__shfl_xor_sync(0xffffffffu, best.hi, off),
-                      __shfl_xor_sync(0xffffffffu, best.lo, off)};
-                int os = __shfl_xor_sync(0xffffffffu, best_slot, off);
-                if (os >= 0 && (best_slot < 0 || key_less(o, best) ||
-                                (o.hi == best.hi && o.lo == best.lo && os < best_slot))) {
-                    best = o;
-                    best_slot = os;
-                }
-            }
-            if (best_slot < 0) break;  // frontier empty
-            const float s = sm.f_score[best_slot];
-            if (s == -INFINITY) break;  // everything left is -inf
-            const int d = sm.f_depth[best_slot];
-            const uint64_t path = sm.f_path[best_slot];
-            const int pnode = sm.f_parent[best_slot];
+            const int win = __ffs(tied) - 1;
+            // ---- the popped candidate, to every lane
+            const float s = __shfl_sync(kAll, mine.score, win);
+            const int d = __shfl_sync(kAll, mine.depth, win);
+            const uint64_t path = (static_cast<uint64_t>(__shfl_sync(kAll, static_cast<uint32_t>(mine.path >> 32), win))
+                                   << 32) |
+                                  __shfl_sync(kAll, static_cast<uint32_t>(mine.path), win);
             const int shift = 4 * (16 - d);
             const int r = static_cast<int>((path >> shift) & 15ull);
             const bool has_sibling = r + 1 < K;
             const bool has_child = d < D;
-            // the popped slot becomes the next sibling (same parent, rank r+1);
-            // the first child (depth d+1, rank 0) takes the popped slot when
-            // there is no sibling, else the lowest free slot, found by the warp
-            int child_slot = best_slot;
-            if (has_child && has_sibling) {
-                int mine = 0x7fffffff;
-                for (int k = 0; k < kFrontierSlots; ++k)
-                    if (!sm.f_valid[lane * kFrontierSlots + k]) {
-                        mine = lane * kFrontierSlots + k;
-                        break;
-                    }
-                for (int off = 16; off > 0; off >>= 1) mine = min(mine, __shfl_xor_sync(0xffffffffu, mine, off));
-                child_slot = mine;  // exists: at most budget+1 <= 65 live entries
-            }
-            __syncwarp();
-            if (lane == 0) {
-                const int i = n;
+            const int i = n;  // the new node's index
+            // the first child goes to the popped slot when there is no
+            // sibling, else to the lowest free slot of the lowest lane with one
+            int free_k = -1;
+#pragma unroll
+            for (int k = kFrontierSlots - 1; k >= 0; --k)
+                if (f[k].key == kNoKey) free_k = k;
+            const unsigned has_free = __ballot_sync(kAll, free_k >= 0);
+            const int child_lane = has_sibling ? __ffs(has_free) - 1 : win;
+            if (lane == win) {
+                const int pnode = mine.parent;
                 sm.n_score[i] = s;
                 sm.n_parent[i] = pnode;
                 sm.n_depth[i] = d;
                 sm.n_rank[i] = r;
                 sm.n_token[i] = sm.d_tok[(d - 1) * K + r];
-                sm.n_mask[i][0] = sm.n_mask[pnode][0];
-                sm.n_mask[i][1] = sm.n_mask[pnode][1];
-                sm.n_mask[i][i >> 6] |= 1ull << (i & 63);
-                if (has_sibling) {
-                    sm.f_score[best_slot] = __fadd_rn(sm.n_score[pnode], sm.d_lp[(d - 1) * K + r + 1]);
-                    sm.f_path[best_slot] = path + (1ull << shift);
-                } else if (!has_child) {
-                    sm.f_valid[best_slot] = 0;
+                uint64_t m0 = sm.n_mask[pnode][0], m1 = sm.n_mask[pnode][1];
+                if (i < 64) m0 |= 1ull << i;
+                else m1 |= 1ull << (i - 64);
+                sm.n_mask[i][0] = m0;
+                sm.n_mask[i][1] = m1;
+                // the popped slot becomes the next sibling (same parent, rank r+1)
+#pragma unroll
+                for (int k = 0; k < kFrontierSlots; ++k) {
+                    if (k != ls) continue;
+                    if (has_sibling) {
+                        f[k].score = __fadd_rn(mine.pscore, sm.d_lp[(d - 1) * K + r + 1]);
+                        f[k].key = score_key(f[k].score);
+                        f[k].path = path + (1ull << shift);
+                    } else {
+                        f[k].key = kNoKey;
+                    }
                 }
-                if (has_child) {
-                    sm.f_valid[child_slot] = 1;
-                    sm.f_score[child_slot] = __fadd_rn(s, sm.d_lp[d * K + 0]);
-                    sm.f_path[child_slot] = path;
-                    sm.f_depth[child_slot] = d + 1;
-                    sm.f_parent[child_slot] = i;
-                }
+            }
+            if (has_child && lane == child_lane) {
+                const int k_child = has_sibling ? free_k : ls;
+                const float cs = __fadd_rn(s, sm.d_lp[d * K + 0]);
+#pragma unroll
+                for (int k = 0; k < kFrontierSlots; ++k)
+                    if (k == k_child) f[k] = Slot{score_key(cs), cs, s, d + 1, i, path};
             }
             ++n;
             __syncwarp();

@@ -84,6 +84,8 @@ constexpr int kOffSX = kOffRing + kSlots * kSlotBytes;            // 196608: the
 constexpr int kSXBytes = kRows * kKeys * 4;                       // 32768
 constexpr int kOffBar = kOffSX + kSXBytes;                        // 229376: barriers and flags (256 B)
 constexpr int kSmemBytes = kOffBar + 256 + 1024;                  // + alignment slack
+constexpr int kOutBoxBytes = kRows * 128;                         // output staging: 128 rows x 32 fp32
+static_assert(8 * kOutBoxBytes <= kSlots * kSlotBytes, "output staging must fit in the KV ring");
 
 // tensor memory columns
 constexpr uint32_t kColO = 0;       // 256: this CTA's half of O
@@ -117,6 +119,14 @@ enum {
     BAR_MAXX = 23,       // 4
     NUM_BARS = 27
 };
+
+// arrival count of barrier i (see the enum)
+__device__ __forceinline__ uint32_t bar_count(int i) {
+    if (i == BAR_QT_READY || (i >= BAR_P_FULL && i < BAR_P_FULL + kSPBufs)) return 8;  // one per softmax warp
+    if (i == BAR_SX_EMPTY) return 2 * kRows;  // every partner softmax thread
+    if (i >= BAR_MAXX && i < BAR_MAXX + 4) return 2;  // warps q and q+4
+    return 1;  // one arrival (SX_FULL: the arming thread; its bytes come from the partner's st.async)
+}
 
 struct AttnArgs {
     int B, Qc, W, H, Tcap, nsplit;
@@ -157,7 +167,8 @@ __device__ __noinline__ uint32_t half_tile_visibility(int key0, int T, int n, ui
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                       const __grid_constant__ CUtensorMap tm_kr, const AttnArgs a) {
+                       const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_o,
+                       const AttnArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -167,10 +178,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int chunk = blockIdx.y;
     const int b = blockIdx.z;
 
-    // ---- per-sequence key range (uniform over the cluster)
-    const int T = a.prefix_len[b];
-    int n = a.n_nodes[b];
-    n = n < 1 ? 1 : (n > a.Qc ? a.Qc : n);
+    // ---- per-sequence key range (uniform over the cluster). The two loads
+    // are issued here and first used after the barrier / tensor-memory /
+    // cluster setup below, which hides their latency.
+    const int T_in = a.prefix_len[b];
+    const int n_in = a.n_nodes[b];
+    // Each softmax thread's part of its row's query that tensor memory holds
+    // (latent chunk 3 for key-half-0 warps, the rotary query for key-half-1
+    // warps), loaded here for the same reason.
+    uint32_t q_pre[32];
+#pragma unroll
+    for (int v = 0; v < 32; ++v) q_pre[v] = 0;
+    if (warp < 8) {
+        const int g_pre = mt * kRows + (warp & 3) * 32 + lane;
+        if (g_pre < a.Qc * a.H) {
+            const size_t r_pre = static_cast<size_t>(b) * a.Qc * a.H + g_pre;
+            const uint4 *src = (warp >> 2) == 0
+                                   ? reinterpret_cast<const uint4 *>(a.q_lat + r_pre * 512 + rank * 256 + 192)
+                                   : reinterpret_cast<const uint4 *>(a.q_rope + r_pre * 64 + rank * 32);
+            const int nv = (warp >> 2) == 0 ? 8 : 4;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                if (v < nv) {
+                    const uint4 x = src[v];
+                    q_pre[4 * v] = x.x;
+                    q_pre[4 * v + 1] = x.y;
+                    q_pre[4 * v + 2] = x.z;
+                    q_pre[4 * v + 3] = x.w;
+                }
+            }
+        }
+    }
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + kOffQ, sRing = sbase + kOffRing;
+    const uint32_t sBar = sbase + kOffBar;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + NUM_BARS * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + NUM_BARS * 8 + 4);
+    // (the word after it is a scratch target for dependency stores)
+    auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
+
+    // Setup. The producer warp initialises the barriers (one per lane) and
+    // starts the query load at once; the MMA warp allocates tensor memory
+    // meanwhile. A CTA barrier publishes both locally. The cluster barrier
+    // that makes this CTA's barriers safe for the partner to touch is only
+    // arrived on here (relaxed: the init fence already releases the inits);
+    // the softmax threads wait on it just before their first remote store.
+    if (warp == kProducerWarp) {
+        if (lane < NUM_BARS) mbar_init(bar(lane), bar_count(lane));
+        if (lane == 0) *abort_flag = 0;
+        mbar_fence_init();
+        __syncwarp();
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_kv);
+            tma_prefetch_desc(&tm_kr);
+            const int qrow = b * a.Qc * a.H + mt * kRows;
+            mbar_arrive_expect_tx(bar(BAR_Q_FULL), kQSmemChunks * kChunkBytesQ);
+            for (int c = 0; c < kQSmemChunks; ++c)
+                tma_load_2d(sQ + c * kChunkBytesQ, &tm_q, static_cast<int>(rank) * 256 + c * 64, qrow,
+                            bar(BAR_Q_FULL));
+        }
+    } else if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_arrive_relaxed();
+    const uint32_t tmem = *tmem_slot;
+    const uint64_t deadline = globaltimer_ns() + a.wait_ns;
+    const int T = T_in;
+    const int n = n_in < 1 ? 1 : (n_in > a.Qc ? a.Qc : n_in);
     const bool seq_ok = (T >= 0) && (static_cast<long long>(T) + n <= a.Tcap);
     const int kend = seq_ok ? T + n : 0;
     const int ntiles = (kend + kKeys - 1) / kKeys;
@@ -184,6 +265,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (!seq_ok && tid == 0 && mt == 0 && rank == 0 && chunk == 0) a.status[b] = DDT_E_BADINPUT;
 
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        a.status[b] = DDT_E_TIMEOUT;
+    };
+
+    float *lse_out = nullptr;  // set by the softmax threads that write an lse
+    float lse_val = 0.f;
     if (nt <= 0) {
         // nothing visible in this range: zero rows (this CTA's half), lse = -inf
         for (int idx = tid; idx < kRows * 64; idx += kThreads) {
@@ -194,68 +283,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *dst = make_float4(0.f, 0.f, 0.f, 0.f);
             if (rank == 0 && c4 == 0) lse_dst[row_base + g] = -INFINITY;
         }
-        return;  // both CTAs of the cluster leave here together
-    }
-
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + kOffQ, sRing = sbase + kOffRing;
-    const uint32_t sBar = sbase + kOffBar;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + NUM_BARS * 8);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + NUM_BARS * 8 + 4);
-    // (the word after it is a scratch target for dependency stores)
-    auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
-
-    if (tid == 0) {
-        mbar_init(bar(BAR_Q_FULL), 1);
-        mbar_init(bar(BAR_QT_READY), 8);
-        for (int s = 0; s < kSlots; ++s) {
-            mbar_init(bar(BAR_RING_FULL + s), 1);
-            mbar_init(bar(BAR_RING_EMPTY + s), 1);
+        if (warp == kProducerWarp && lane == 0) {
+            const int zero = 0;
+            mbar_wait(bar(BAR_Q_FULL), 0, globaltimer_ns() + 100000000ull, &zero);
         }
-        for (int s = 0; s < kSPBufs; ++s) {
-            mbar_init(bar(BAR_S_FULL + s), 1);
-            mbar_init(bar(BAR_P_FULL + s), 8);
-            mbar_init(bar(BAR_PV_DONE + s), 1);
-        }
-        mbar_init(bar(BAR_O_FINAL), 1);
-        mbar_init(bar(BAR_DRAIN), 1);
-        // SX_FULL completes on bytes: one local thread arms each phase with
-        // expect_tx and the partner's st.async credits the bytes
-        mbar_init(bar(BAR_SX_FULL), 1);
-        mbar_init(bar(BAR_SX_EMPTY), 2 * kRows);
-        for (int q = 0; q < 4; ++q) mbar_init(bar(BAR_MAXX + q), 2);  // warps q and q+4
-        *abort_flag = 0;
-        mbar_fence_init();
-    }
-    if (warp == kMmaWarp) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    // both CTAs' barriers must exist before either sends the other anything
-    cluster_sync();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint64_t deadline = globaltimer_ns() + a.wait_ns;
-
-    auto fail = [&]() {
-        *abort_flag = 1;
-        a.status[b] = DDT_E_TIMEOUT;
-    };
-
-    if (warp == kProducerWarp) {
+    } else if (warp == kProducerWarp) {
         // ======================= TMA producer =======================
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_kv);
-            tma_prefetch_desc(&tm_kr);
-            const int qrow = static_cast<int>(row_base) + mt * kRows;
-            mbar_arrive_expect_tx(bar(BAR_Q_FULL), kQSmemChunks * kChunkBytesQ);
-            for (int c = 0; c < kQSmemChunks; ++c)
-                tma_load_2d(sQ + c * kChunkBytesQ, &tm_q, static_cast<int>(rank) * 256 + c * 64, qrow,
-                            bar(BAR_Q_FULL));
             int armed[kSlots] = {0, 0, 0, 0};
             bool ok = true;
             for (int jj = 0; jj < nt; ++jj) {
@@ -451,27 +485,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // this row's latent query chunk 3 (key-half-0 warps) or rotary query
         // (key-half-1 warps) -> tensor memory, as bf16 pairs (low half = even column)
         {
-            uint32_t q[32];
-#pragma unroll
-            for (int v = 0; v < 32; ++v) q[v] = 0;
-            if (row_in_seq) {
-                const uint4 *src =
-                    half == 0 ? reinterpret_cast<const uint4 *>(a.q_lat + (row_base + g) * 512 + rank * 256 + 192)
-                              : reinterpret_cast<const uint4 *>(a.q_rope + (row_base + g) * 64 + rank * 32);
-                const int nv = half == 0 ? 8 : 4;
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    if (v < nv) {
-                        const uint4 x = src[v];
-                        q[4 * v] = x.x;
-                        q[4 * v + 1] = x.y;
-                        q[4 * v + 2] = x.z;
-                        q[4 * v + 3] = x.w;
-                    }
-                }
-            }
-            if (half == 0) tmem_st32(tmem + lane_base + kColQ3, q);
-            else tmem_st16(tmem + lane_base + kColQR, *reinterpret_cast<const uint32_t(*)[16]>(&q[0]));
+            if (half == 0) tmem_st32(tmem + lane_base + kColQ3, q_pre);
+            else tmem_st16(tmem + lane_base + kColQR, *reinterpret_cast<const uint32_t(*)[16]>(&q_pre[0]));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -500,7 +515,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // The partial of tile t+1 is loaded and shipped before the softmax of
         // tile t, so its transfer to the partner overlaps that softmax.
         uint32_t sv[32];
-        if (!load_own(0, sv)) ok = false;
+        const bool ok0 = load_own(0, sv);
+        // the partner's barriers exist before this CTA's first remote operation
+        cluster_wait();
+        if (!ok0) ok = false;
         else ship(sv);
         for (int jj = 0; jj < nt && ok; ++jj) {
             const int sb = jj % kSPBufs;
@@ -625,34 +643,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             tc_fence_after();
             const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-            float *dst = o_dst + (row_base + g) * 512 + rank * 256 + half * 128;
+            // Stage this thread's 128 output columns in the KV ring (idle once
+            // every PV is done) as four of the eight 128-row x 32-column fp32
+            // boxes of this CTA's half, in the 128-byte swizzle (16-byte chunk
+            // j of row r at chunk j ^ (r % 8)) that the tensor store reads.
+            // Written this way each warp store is conflict-free, where direct
+            // row-strided global stores cost a transaction per lane.
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tmem + lane_base + kColO + half * 128 + c * 32, o);
                 tmem_wait_ld();
-                if (row_in_seq) {
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+                uint8_t *box_row = smem + kOffRing + (half * 4 + c) * kOutBoxBytes + row * 128;
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        d4[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                            __uint_as_float(o[4 * v + 2]) * inv_l,
-                                            __uint_as_float(o[4 * v + 3]) * inv_l);
-                }
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4 *>(box_row + ((j ^ (row & 7)) << 4)) =
+                        make_float4(__uint_as_float(o[4 * j]) * inv_l, __uint_as_float(o[4 * j + 1]) * inv_l,
+                                    __uint_as_float(o[4 * j + 2]) * inv_l, __uint_as_float(o[4 * j + 3]) * inv_l);
             }
+            fence_proxy_async_smem();
             // both CTAs hold the same row sum and max; one writes the lse
-            if (rank == 0 && half == 0 && row_in_seq)
-                lse_dst[row_base + g] = l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+            // (after the final cluster barrier, like the output block)
+            if (rank == 0 && half == 0 && row_in_seq) {
+                lse_out = lse_dst + row_base + g;
+                lse_val = l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+            }
         }
     }
 
+    // (threads that did not wait on the setup's cluster barrier do it now)
+    if (warp >= kProducerWarp || nt <= 0) cluster_wait();
     tc_fence_before();
-    // neither CTA may leave while its partner can still write into it
+    // every softmax warp has staged its part of the output block: one thread
+    // stores the CTA's 128 x 256 block; the tensor map has the sequence's rows
+    // as one dimension, so rows past the sequence are not written
+    __syncthreads();
+    const bool store_out = tid == 0 && nt > 0 && !*abort_flag;
+    if (store_out) {
+        for (int c = 0; c < 8; ++c)
+            tma_store_3d(&tm_o, sRing + c * kOutBoxBytes, static_cast<int>(rank) * 256 + c * 32, mt * kRows,
+                         b + a.B * chunk);
+        bulk_commit_group();
+    }
+    // Neither CTA may leave while its partner can still write into it. The
+    // lse stores come after this barrier so its release arrivals do not wait
+    // for them.
     cluster_sync();
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    if (lse_out) *lse_out = lse_val;
+    if (store_out) bulk_wait_read_all();
 }
 
 // Merge per-chunk normalised partials: lse = log sum_c exp(lse_c),
@@ -718,6 +760,19 @@ bool encode_2d(EncodeTiledFn enc, CUtensorMap *m, const void *ptr, uint64_t cols
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp32 tensor [dim2][dim1][cols] row-major, box [box_rows, 32 columns] (128 bytes,
+// 128-byte swizzle), for tile stores
+bool encode_3d_f32_store(EncodeTiledFn enc, CUtensorMap *m, void *ptr, uint64_t cols, uint64_t dim1,
+                         uint64_t dim2, uint32_t box_rows) {
+    cuuint64_t dims[3] = {cols, dim1, dim2};
+    cuuint64_t strides[2] = {cols * 4, dim1 * cols * 4};
+    cuuint32_t box[3] = {32, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -801,8 +856,13 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
         a.o_dst = out.out;
         a.lse_dst = out.lse;
     }
+    // the output (or the key-range partials) as [splits x B][Qc*H rows][512]
+    CUtensorMap tm_o;
+    if (!encode_3d_f32_store(enc, &tm_o, a.o_dst, 512, static_cast<uint64_t>(tree.Qc) * in.H,
+                             static_cast<uint64_t>(tree.B) * plan.nsplit, kRows))
+        return DDT_E_INVAL;
     dim3 grid(plan.mtiles * 2, plan.nsplit, tree.B);
-    verify_attn_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_q, tm_kv, tm_kr, a);
+    verify_attn_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_q, tm_kv, tm_kr, tm_o, a);
     if (cudaGetLastError() != cudaSuccess) return DDT_E_CUDA;
     if (plan.nsplit > 1) {
         merge_chunks_kernel<<<static_cast<unsigned>(rows_total), 128, 0, s>>>(
