@@ -150,8 +150,11 @@ int ddt_verify_step(const ddt_draft *draft, int budget, ddt_tree *tree, const dd
     if (plan.ws_bytes > ws_bytes || (plan.ws_bytes && !workspace)) return DDT_E_INVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (ddt::launch_tree_build(*draft, budget, *tree, s) != cudaSuccess) return DDT_E_CUDA;
-    if (int rc = ddt::launch_verify_attn(*attn, *tree, scale, *attn_out, workspace, ws_bytes, plan, s)) return rc;
-    if (ddt::launch_tree_accept(*tree, target_argmax, *acc, s) != cudaSuccess) return DDT_E_CUDA;
+    // the attention starts while the tree is being built (it waits, in the
+    // kernel, before it reads the tree); the accept runs beside the merge
+    if (int rc = ddt::launch_verify_attn(*attn, *tree, scale, *attn_out, workspace, ws_bytes, plan, s, true))
+        return rc;
+    if (ddt::launch_tree_accept(*tree, target_argmax, *acc, s, true) != cudaSuccess) return DDT_E_CUDA;
     return DDT_OK;
 }
 

@@ -14,8 +14,12 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 cudaError_t launch_tree_build(const ddt_draft &in, int budget, const ddt_tree &out,
                               cudaStream_t s);
+// With `after_prev` the kernel is launched with programmatic stream
+// serialization: it may start before the previous kernel on the stream ends.
+// Only the verify step chains its kernels this way (each kernel waits, in
+// its code, for the data it needs); standalone calls launch normally.
 cudaError_t launch_tree_accept(const ddt_tree &tree, const int32_t *target,
-                               const ddt_accept &out, cudaStream_t s);
+                               const ddt_accept &out, cudaStream_t s, bool after_prev = false);
 
 struct AttnPlan {
     int mtiles;       // 128-row tiles of Qc*H rows per sequence
@@ -30,7 +34,27 @@ AttnPlan plan_attention(int B, int Qc, int H, int Tcap, int sms);
 // kernel when nsplit > 1).
 int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
                        const ddt_attn_out &out, void *workspace, size_t ws_bytes,
-                       const AttnPlan &plan, cudaStream_t s);
+                       const AttnPlan &plan, cudaStream_t s, bool after_prev = false);
+
+// cudaLaunchKernelEx with the programmatic-stream-serialization attribute
+// when `after_prev`, a plain launch otherwise.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          bool after_prev, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (after_prev) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 cudaError_t launch_selftest_wait(int32_t *status, unsigned timeout_us, cudaStream_t s);
 

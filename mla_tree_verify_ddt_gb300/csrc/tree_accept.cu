@@ -78,17 +78,21 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
         accept_len[b] = len;
         next_root[b] = t;
     }
+    // In a verify step this kernel may run beside the attention's merge
+    // (it needs only the tree); it ends after the kernel before it, so that
+    // work later on the stream also follows that one.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
 
 cudaError_t launch_tree_accept(const ddt_tree &tree, const int32_t *target,
-                               const ddt_accept &out, cudaStream_t s) {
+                               const ddt_accept &out, cudaStream_t s, bool after_prev) {
     const int blocks = (tree.B + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    tree_accept_kernel<<<blocks, 32 * kWarpsPerBlock, 0, s>>>(
-        tree.B, tree.D, tree.Qc, tree.token, tree.parent, tree.n_nodes, target, out.accept_len,
-        out.accept_idx, out.commit_tok, out.next_root);
-    return cudaGetLastError();
+    return launch_kernel(tree_accept_kernel, dim3(blocks), dim3(32 * kWarpsPerBlock), 0, s, after_prev, tree.B,
+                         tree.D, tree.Qc, static_cast<const int32_t *>(tree.token),
+                         static_cast<const int32_t *>(tree.parent), static_cast<const int32_t *>(tree.n_nodes),
+                         target, out.accept_len, out.accept_idx, out.commit_tok, out.next_root);
 }
 
 }  // namespace ddt

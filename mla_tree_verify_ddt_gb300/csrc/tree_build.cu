@@ -84,6 +84,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
                       uint64_t *__restrict__ o_mask, int32_t *__restrict__ o_n_nodes,
                       int32_t *__restrict__ o_status) {
     __shared__ WarpSmem sm_all[kWarpsPerBlock];
+    // the attention kernel of a verify step may start at once: it streams
+    // the prefix before it needs the tree
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * kWarpsPerBlock + warp;
     if (b >= B) return;

@@ -83,7 +83,10 @@ constexpr int kOffRing = kOffQ + kQSmemChunks * kChunkBytesQ;     // 49152
 constexpr int kOffSX = kOffRing + kSlots * kSlotBytes;            // 196608: the partner's partial S of a tile
 constexpr int kSXBytes = kRows * kKeys * 4;                       // 32768
 constexpr int kOffBar = kOffSX + kSXBytes;                        // 229376: barriers and flags (256 B)
-constexpr int kSmemBytes = kOffBar + 256 + 1024;                  // + alignment slack
+constexpr int kOffTree = kOffBar + 256;                           // 229632: the tree as this CTA needs it
+constexpr int kMaxTileNodes = DDT_MAX_BUDGET + 1;                 // nodes a 128-row tile can span (<= Qc)
+constexpr int kTreeBytes = 16 + kMaxTileNodes * 16;               // node count, then 2 mask words per node
+constexpr int kSmemBytes = kOffTree + kTreeBytes + 1024;          // + alignment slack
 constexpr int kOutBoxBytes = kRows * 128;                         // output staging: 128 rows x 32 fp32
 static_assert(8 * kOutBoxBytes <= kSlots * kSlotBytes, "output staging must fit in the KV ring");
 
@@ -97,9 +100,10 @@ constexpr uint32_t kColX = 496;     // 4: [round parity][key half] word the two 
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// warps 0-7 softmax group (two threads per row), 8 TMA producer, 9 MMA issuer
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+// warps 0-7 softmax group (two threads per row), 8 TMA producer, 9 MMA issuer,
+// 10 tree fetch (it waits for the tree build, which stalls its whole warp)
+constexpr int kThreads = 352;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kTreeWarp = 10;
 
 enum {
     BAR_Q_FULL = 0,
@@ -117,7 +121,8 @@ enum {
     // the two threads of a row swap their halves' tile max (and, at the end,
     // their row sums): one barrier per TMEM lane quadrant
     BAR_MAXX = 23,       // 4
-    NUM_BARS = 27
+    BAR_TREE = 27,       // the tree's node count and this tile's node masks are in shared memory
+    NUM_BARS = 28
 };
 
 // arrival count of barrier i (see the enum)
@@ -182,7 +187,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // are issued here and first used after the barrier / tensor-memory /
     // cluster setup below, which hides their latency.
     const int T_in = a.prefix_len[b];
-    const int n_in = a.n_nodes[b];
     // Each softmax thread's part of its row's query that tensor memory holds
     // (latent chunk 3 for key-half-0 warps, the rotary query for key-half-1
     // warps), loaded here for the same reason.
@@ -250,30 +254,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_arrive_relaxed();
     const uint32_t tmem = *tmem_slot;
     const uint64_t deadline = globaltimer_ns() + a.wait_ns;
+    // Key ranges are cut from the prefix length and the node capacity alone,
+    // not from the tree's node count. The tiles wholly inside the prefix are
+    // then known at once and can be streamed while the previous kernel (the
+    // tree build, under programmatic dependent launch) is still running; the
+    // tree is read between the two phases of each role's tile loop: the
+    // tiles known without it, then the rest.
     const int T = T_in;
-    const int n = n_in < 1 ? 1 : (n_in > a.Qc ? a.Qc : n_in);
-    const bool seq_ok = (T >= 0) && (static_cast<long long>(T) + n <= a.Tcap);
-    const int kend = seq_ok ? T + n : 0;
-    const int ntiles = (kend + kKeys - 1) / kKeys;
+    const bool t_ok = T >= 0 && T < a.Tcap;
+    const int kcap = t_ok ? (a.Tcap - T < a.Qc ? a.Tcap : T + a.Qc) : 0;
+    const int ntiles = (kcap + kKeys - 1) / kKeys;
     const int t0 = static_cast<int>((static_cast<long long>(ntiles) * chunk) / a.nsplit);
     const int t1 = static_cast<int>((static_cast<long long>(ntiles) * (chunk + 1)) / a.nsplit);
-    const int nt = t1 - t0;
+    const int nrange = t1 - t0;
     const int rows_seq = a.Qc * a.H;
     const size_t row_base = static_cast<size_t>(b) * rows_seq;
     float *o_dst = a.o_dst + static_cast<size_t>(chunk) * a.rows_total * 512;
     float *lse_dst = a.lse_dst + static_cast<size_t>(chunk) * a.rows_total;
 
-    if (!seq_ok && tid == 0 && mt == 0 && rank == 0 && chunk == 0) a.status[b] = DDT_E_BADINPUT;
-
-
     auto fail = [&]() {
         *abort_flag = 1;
+        grid_dep_wait();  // after the tree build's own status write
         a.status[b] = DDT_E_TIMEOUT;
     };
 
+    // Known once the tree is: the node count, whether prefix + nodes fit the
+    // key capacity, and the sequence's key end. Only the softmax needs them
+    // (for tiles that reach past the prefix, and at the end); the tree-fetch
+    // warp copies the node count and the ancestor masks of this tile's nodes
+    // into shared memory once the tree build has finished. Tiles of the range
+    // past the key end (at most one, when the tree is not full) are processed
+    // fully masked.
+    const volatile int *tree_n = reinterpret_cast<const volatile int *>(smem + kOffTree);
+    const uint64_t *tree_mask = reinterpret_cast<const uint64_t *>(smem + kOffTree + 16);
+    const int node_lo = (mt * kRows) / a.H;  // first node of the tile's rows
+    int n = 1, kend = 0;
+    bool seq_ok = false, resolved = false;
+    // (tree_ready false: a bounded wait for the tree ran out; the CTA stops)
+    auto resolve = [&](bool tree_ready, int n_in) {
+        if (!tree_ready) fail();
+        n = n_in < 1 ? 1 : (n_in > a.Qc ? a.Qc : n_in);
+        seq_ok = tree_ready && t_ok && static_cast<long long>(T) + n <= a.Tcap;
+        kend = seq_ok ? T + n : 0;
+        resolved = true;
+    };
+
+
     float *lse_out = nullptr;  // set by the softmax threads that write an lse
     float lse_val = 0.f;
-    if (nt <= 0) {
+    if (nrange <= 0) {
         // nothing visible in this range: zero rows (this CTA's half), lse = -inf
         for (int idx = tid; idx < kRows * 64; idx += kThreads) {
             const int r = idx >> 6, c4 = idx & 63;
@@ -292,7 +321,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int armed[kSlots] = {0, 0, 0, 0};
             bool ok = true;
-            for (int jj = 0; jj < nt; ++jj) {
+            for (int jj = 0; jj < nrange; ++jj) {
                 const int slot = jj % kSlots, use = jj / kSlots;
                 if (use >= 1 && !mbar_wait(bar(BAR_RING_EMPTY + slot), (use - 1) & 1, deadline, abort_flag)) {
                     ok = false;
@@ -318,6 +347,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (armed[s]) mbar_wait(bar(BAR_RING_FULL + s), (armed[s] - 1) & 1, drain_deadline, &zero);
             }
         }
+    } else if (warp == kTreeWarp) {
+        // ======================= tree fetch =======================
+        // the node count and the ancestor masks of this tile's nodes, once
+        // the tree build has finished
+        grid_dep_wait();
+        const int node_hi = min((mt * kRows + kRows - 1) / a.H, a.Qc - 1);
+        const uint64_t *src = a.mask + (static_cast<size_t>(b) * a.Qc + node_lo) * a.W;
+        uint64_t *dst = reinterpret_cast<uint64_t *>(smem + kOffTree + 16);
+        const int words = (node_hi - node_lo + 1) * a.W;
+        for (int w = lane; w < words; w += 32) dst[(w / a.W) * 2 + (w % a.W)] = src[w];
+        if (lane == 0) *reinterpret_cast<volatile int *>(smem + kOffTree) = a.n_nodes[b];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_TREE));
     } else if (warp == kMmaWarp) {
         // ======================= MMA issuer =======================
         if (lane == 0) {
@@ -353,7 +395,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 return 1;
             };
             auto try_pv = [&]() -> bool {
-                if (pv_next >= nt) return true;
+                if (pv_next >= nrange) return true;
                 const int r = issue_pv(pv_next, false);
                 if (r < 0) return false;
                 pv_next += r;
@@ -365,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             auto wait_feeding_pv = [&](uint32_t barrier, uint32_t parity, int upto) -> bool {
                 for (uint32_t it = 0;; ++it) {
                     if (mbar_try_wait(barrier, parity)) return true;
-                    if (pv_next < upto && pv_next < nt) {
+                    if (pv_next < upto && pv_next < nrange) {
                         const int r = issue_pv(pv_next, false);
                         if (r < 0) return false;
                         pv_next += r;
@@ -373,7 +415,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if ((it & 63u) == 63u && (*abort_flag || globaltimer_ns() > deadline)) return false;
                 }
             };
-            for (int jj = 0; jj < nt && ok; ++jj) {
+            for (int jj = 0; jj < nrange && ok; ++jj) {
                 const int sb = jj % kSPBufs, slot = jj % kSlots;
                 // a PV that became ready goes first
                 if (pv_next < jj && !try_pv()) {
@@ -412,7 +454,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     else ++pv_next;
                 }
             }
-            while (ok && pv_next < nt) {
+            while (ok && pv_next < nrange) {
                 if (issue_pv(pv_next, true) < 0) ok = false;
                 else ++pv_next;
             }
@@ -440,14 +482,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int g = mt * kRows + row;              // row within the sequence
         const bool row_in_seq = g < rows_seq;
         const int node = g / a.H;
-        const bool node_ok = row_in_seq && node < n && seq_ok;
+        // Until the tree is known every in-sequence row is treated as a node:
+        // the tiles processed before that are pure prefix, visible to all
+        // nodes, and rows of absent nodes come out zero in the end.
+        bool node_ok = row_in_seq;
+        const int t_tree = (T / kKeys) - t0;  // first tile of the range that can hold node keys
         const bool lead = row == 0 && half == 0;     // arms each tile's SX byte count
         uint64_t m0 = 0, m1 = 0;
-        if (node_ok) {
-            const uint64_t *mk = a.mask + (static_cast<size_t>(b) * a.Qc + node) * a.W;
-            m0 = mk[0];
-            if (a.W > 1) m1 = mk[1];
-        }
+        auto resolve_s = [&]() -> bool {
+            const bool ready = __all_sync(0xffffffffu, mbar_wait(bar(BAR_TREE), 0, deadline, abort_flag));
+            resolve(ready, ready ? *tree_n : 0);
+            node_ok = row_in_seq && node < n && seq_ok;
+            if (node_ok) {
+                m0 = tree_mask[(node - node_lo) * 2];
+                if (a.W > 1) m1 = tree_mask[(node - node_lo) * 2 + 1];
+            }
+            return ready;
+        };
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t col_half = static_cast<uint32_t>(half) * 32;   // this thread's 32 columns of an S/P buffer
         const uint4 *sx = reinterpret_cast<const uint4 *>(smem + kOffSX);   // [16 groups][128 rows] of 4 floats
@@ -520,7 +571,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         cluster_wait();
         if (!ok0) ok = false;
         else ship(sv);
-        for (int jj = 0; jj < nt && ok; ++jj) {
+        for (int jj = 0; jj < nrange && ok; ++jj) {
             const int sb = jj % kSPBufs;
             const int key0 = (t0 + jj) * kKeys + half * 32;
             // ---- the partner's partial of tile jj: 128 rows x 256 B
@@ -548,7 +599,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // has read this tile's. The eight stores are spread over the
             // softmax below: the link to the partner drains at a few tens of
             // GB/s, and a burst of them would stall this thread until it has.
-            const bool ship_next = jj + 1 < nt;
+            const bool ship_next = jj + 1 < nrange;
             if (ship_next && (!load_own(jj + 1, sv) || !wwait_cluster(bar(BAR_SX_EMPTY), jj & 1))) {
                 ok = false;
                 break;
@@ -559,6 +610,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 make_uint4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]), r_bar_sx_full);
             };
             // ---- masked online softmax, log2 domain
+            if (!resolved && jj >= t_tree && !resolve_s()) {
+                ok = false;
+                break;
+            }
             uint32_t vis = ~0u;
             if (!node_ok) vis = 0;
             else if (key0 + 32 > T) vis = half_tile_visibility(key0, T, n, m0, m1);
@@ -618,7 +673,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // KV rows past the last node may hold anything (NaN included) and
             // P is 0 there, but 0 * NaN is NaN: zero those V rows of the tail
             // tile (S, which read them as K, is already complete)
-            if ((t0 + jj) * kKeys + kKeys > kend) {
+            if (jj >= t_tree && (t0 + jj) * kKeys + kKeys > kend) {  // (jj >= t_tree: the tree is known)
                 uint4 *vset = reinterpret_cast<uint4 *>(smem + kOffRing + (jj % kSlots) * kSlotBytes);
                 const int kvalid = kend - (t0 + jj) * kKeys;
 #pragma unroll 1
@@ -632,9 +687,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(BAR_P_FULL + sb));
         }
+        if (ok && !resolved && !resolve_s()) ok = false;
         // the row sum is the two halves' sums (same reference max)
         float l_other;
-        if (ok && !swap_with_other_half(nt, l_sum, l_other)) ok = false;
+        if (ok && !swap_with_other_half(nrange, l_sum, l_other)) ok = false;
         if (ok) l_sum += l_other;
         if (ok && !wwait(bar(BAR_O_FINAL), 0)) ok = false;
         if (!ok) {
@@ -642,7 +698,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else {
             __syncwarp();
             tc_fence_after();
-            const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+            // rows of absent nodes, and every row of a range with no tile of
+            // this sequence's keys, are zero (tensor memory was not written)
+            const bool zero_row = !node_ok;
+            const float inv_l = (l_sum > 0.f && !zero_row) ? 1.0f / l_sum : 0.f;
             // Stage this thread's 128 output columns in the KV ring (idle once
             // every PV is done) as four of the eight 128-row x 32-column fp32
             // boxes of this CTA's half, in the 128-byte swizzle (16-byte chunk
@@ -655,6 +714,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_ld32(tmem + lane_base + kColO + half * 128 + c * 32, o);
                 tmem_wait_ld();
                 uint8_t *box_row = smem + kOffRing + (half * 4 + c) * kOutBoxBytes + row * 128;
+                if (zero_row) {
+#pragma unroll
+                    for (int v = 0; v < 32; ++v) o[v] = 0u;
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     *reinterpret_cast<float4 *>(box_row + ((j ^ (row & 7)) << 4)) =
@@ -666,19 +729,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // (after the final cluster barrier, like the output block)
             if (rank == 0 && half == 0 && row_in_seq) {
                 lse_out = lse_dst + row_base + g;
-                lse_val = l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+                lse_val = (l_sum > 0.f && !zero_row) ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
             }
         }
     }
 
     // (threads that did not wait on the setup's cluster barrier do it now)
-    if (warp >= kProducerWarp || nt <= 0) cluster_wait();
+    if (warp >= kProducerWarp || nrange <= 0) cluster_wait();
+    // Every thread has waited for the tree build by now (or does so here);
+    // only then may the next kernel of the step start.
+    grid_dep_wait();
+    grid_dep_launch();
+    if (tid == 0) {
+        if (!resolved) {
+            if (nrange > 0) {
+                const bool r = mbar_wait(bar(BAR_TREE), 0, deadline, abort_flag);
+                resolve(r, r ? *tree_n : 0);
+            } else {
+                grid_dep_wait();
+                resolve(true, a.n_nodes[b]);
+            }
+        }
+        if (!seq_ok && mt == 0 && rank == 0 && chunk == 0 && !*abort_flag) a.status[b] = DDT_E_BADINPUT;
+    }
     tc_fence_before();
     // every softmax warp has staged its part of the output block: one thread
     // stores the CTA's 128 x 256 block; the tensor map has the sequence's rows
     // as one dimension, so rows past the sequence are not written
     __syncthreads();
-    const bool store_out = tid == 0 && nt > 0 && !*abort_flag;
+    const bool store_out = tid == 0 && nrange > 0 && !*abort_flag;
     if (store_out) {
         for (int c = 0; c < 8; ++c)
             tma_store_3d(&tm_o, sRing + c * kOutBoxBytes, static_cast<int>(rank) * 256 + c * 32, mt * kRows,
@@ -703,6 +782,10 @@ __global__ void __launch_bounds__(128)
     merge_chunks_kernel(size_t rows_total, int nsplit, const float *__restrict__ ws_o,
                         const float *__restrict__ ws_lse, float *__restrict__ out,
                         float *__restrict__ lse) {
+    // the accept may start now; the partials are complete once the
+    // attention grid is
+    grid_dep_launch();
+    grid_dep_wait();
     const size_t r = blockIdx.x;
     if (r >= rows_total) return;
     float mx = -INFINITY;
@@ -810,7 +893,7 @@ AttnPlan plan_attention(int B, int Qc, int H, int Tcap, int sms) {
 
 int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
                        const ddt_attn_out &out, void *workspace, size_t ws_bytes,
-                       const AttnPlan &plan, cudaStream_t s) {
+                       const AttnPlan &plan, cudaStream_t s, bool after_prev) {
     EncodeTiledFn enc = get_encoder();
     if (!enc) return DDT_E_CUDA;
     const uint64_t rows_total = static_cast<uint64_t>(tree.B) * tree.Qc * in.H;
@@ -862,12 +945,14 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
                              static_cast<uint64_t>(tree.B) * plan.nsplit, kRows))
         return DDT_E_INVAL;
     dim3 grid(plan.mtiles * 2, plan.nsplit, tree.B);
-    verify_attn_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_q, tm_kv, tm_kr, tm_o, a);
-    if (cudaGetLastError() != cudaSuccess) return DDT_E_CUDA;
+    if (launch_kernel(verify_attn_kernel, grid, dim3(kThreads), kSmemBytes, s, after_prev, tm_q, tm_kv, tm_kr, tm_o,
+                      a) != cudaSuccess)
+        return DDT_E_CUDA;
     if (plan.nsplit > 1) {
-        merge_chunks_kernel<<<static_cast<unsigned>(rows_total), 128, 0, s>>>(
-            rows_total, plan.nsplit, ws_o, ws_lse, out.out, out.lse);
-        if (cudaGetLastError() != cudaSuccess) return DDT_E_CUDA;
+        if (launch_kernel(merge_chunks_kernel, dim3(static_cast<unsigned>(rows_total)), dim3(128), 0, s, after_prev,
+                          static_cast<size_t>(rows_total), plan.nsplit, static_cast<const float *>(ws_o),
+                          static_cast<const float *>(ws_lse), out.out, out.lse) != cudaSuccess)
+            return DDT_E_CUDA;
     }
     return DDT_OK;
 }
