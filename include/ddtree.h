@@ -169,6 +169,24 @@ int ddt_verify_step(const ddt_draft *draft, int budget, ddt_tree *tree,
                     const int32_t *target_argmax, ddt_accept *acc, void *workspace,
                     size_t ws_bytes, void *stream);
 
+/* After accept: the KV append of the committed tokens ("The Architecture of a
+ * Thousand-Parameter Decision: Designing a Native DDTree Inference Engine for
+ * Kimi K2.6", "What to Build New", items 4 and 5: the step ends
+ * draft -> build -> verify -> accept -> append; key layout of "The Milestone
+ * Message", "Architectural Abstraction": node m's key at position L + m).
+ * For each sequence b with T = prefix_len[b] and L = acc->accept_len[b], the
+ * keys of the accepted path acc->accept_idx[b][0..L-1] (node 0, the root, is
+ * already at row T) become rows T .. T+L-1 of c_kv [B,Tcap,512] and k_rope
+ * [B,Tcap,64] (bfloat16 bit patterns, modified in place), and prefix_len[b]
+ * becomes T + L. Rows below T are not touched; rows from T + L on keep
+ * whatever they held. D is the accept rows' length minus one. Host errors:
+ * DDT_E_INVAL for a null pointer, B < 1, D outside [1, DDT_MAX_DEPTH], Tcap
+ * < 1 or a c_kv / k_rope pointer not 16-byte aligned. A sequence whose
+ * accept_len, path indices (must rise from 0) or prefix length do not fit
+ * Tcap is left unchanged and gets DDT_E_BADINPUT in status[b]; no sync. */
+int ddt_kv_commit(const ddt_accept *acc, int B, int D, int Tcap, void *c_kv, void *k_rope,
+                  int32_t *prefix_len, int32_t *status, void *stream);
+
 /* Bytes of device scratch held by ddt_verify_mla_attn_noalloc (64 MiB). */
 #define DDT_NOALLOC_SCRATCH_BYTES (64u << 20)
 

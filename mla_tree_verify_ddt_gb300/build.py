@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libddtree.so")
-SOURCES = ["ddt_api.cu", "tree_build.cu", "tree_accept.cu", "verify_attn.cu", "verify_attn_noalloc.cu"]
+SOURCES = ["ddt_api.cu", "tree_build.cu", "tree_accept.cu", "verify_attn.cu", "verify_attn_noalloc.cu",
+           "kv_commit.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -158,6 +158,19 @@ int ddt_verify_step(const ddt_draft *draft, int budget, ddt_tree *tree, const dd
     return DDT_OK;
 }
 
+int ddt_kv_commit(const ddt_accept *acc, int B, int D, int Tcap, void *c_kv, void *k_rope,
+                  int32_t *prefix_len, int32_t *status, void *stream) {
+    if (!acc || !acc->accept_len || !acc->accept_idx || !c_kv || !k_rope || !prefix_len || !status)
+        return DDT_E_INVAL;
+    if (B < 1 || B > 65535 || D < 1 || D > DDT_MAX_DEPTH || Tcap < 1) return DDT_E_INVAL;
+    if (!aligned16(c_kv) || !aligned16(k_rope)) return DDT_E_INVAL;
+    if (int rc = check_device()) return rc;
+    return ddt::launch_kv_commit(B, D, Tcap, acc->accept_len, acc->accept_idx, c_kv, k_rope, prefix_len, status,
+                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DDT_OK
+               : DDT_E_CUDA;
+}
+
 const char *ddt_status_str(int code) {
     switch (code) {
         case DDT_OK: return "ok";

@@ -56,6 +56,9 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+cudaError_t launch_kv_commit(int B, int D, int Tcap, const int32_t *accept_len, const int32_t *accept_idx,
+                             void *c_kv, void *k_rope, int32_t *prefix_len, int32_t *status, cudaStream_t s);
+
 cudaError_t launch_selftest_wait(int32_t *status, unsigned timeout_us, cudaStream_t s);
 
 }  // namespace ddt

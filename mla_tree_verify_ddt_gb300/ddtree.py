@@ -23,7 +23,7 @@ MAX_DEPTH, MAX_TOPK, MAX_BUDGET, LATENT, ROPE = 16, 16, 64, 512, 64
 
 EXPORTED = ["ddt_workspace_size", "ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept",
             "ddt_verify_step", "ddt_status_str", "ddt_read_device_status",
-            "ddt_selftest_bounded_wait", "ddt_verify_mla_attn_noalloc"]
+            "ddt_selftest_bounded_wait", "ddt_verify_mla_attn_noalloc", "ddt_kv_commit"]
 
 P = ctypes.c_void_p
 I = ctypes.c_int
@@ -82,13 +82,14 @@ def lib() -> ctypes.CDLL:
                                       ctypes.c_size_t, P]
         L.ddt_verify_mla_attn_noalloc.argtypes = [ctypes.POINTER(DdtAttnIn), ctypes.POINTER(DdtTree),
                                                   ctypes.c_float, ctypes.POINTER(DdtAttnOut), P]
+        L.ddt_kv_commit.argtypes = [ctypes.POINTER(DdtAccept), I, I, I, P, P, P, P, P]
         L.ddt_status_str.argtypes = [I]
         L.ddt_status_str.restype = ctypes.c_char_p
         L.ddt_read_device_status.argtypes = [P, I, P]
         L.ddt_selftest_bounded_wait.argtypes = [P, ctypes.c_uint, P]
         for f in ("ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept", "ddt_verify_step",
                   "ddt_read_device_status", "ddt_selftest_bounded_wait",
-                  "ddt_verify_mla_attn_noalloc"):
+                  "ddt_verify_mla_attn_noalloc", "ddt_kv_commit"):
             getattr(L, f).restype = I
         _lib = L
     return _lib
@@ -250,6 +251,19 @@ def ddt_tree_accept(tree: Tree, target_argmax, out: Accept | None = None, stream
     _check(lib().ddt_tree_accept(ctypes.byref(t), _ptr(target_argmax), ctypes.byref(a),
                                  _stream_ptr(stream)), "ddt_tree_accept")
     return out
+
+
+def ddt_kv_commit(acc: Accept, c_kv, k_rope, prefix_len, status, stream=None):
+    """Moves the accepted path's keys into the committed prefix, in place on
+    c_kv [B,Tcap,512] and k_rope [B,Tcap,64] (bf16), and advances prefix_len
+    (int32 [B]); status (int32 [B]) gets DDT_E_BADINPUT for a sequence whose
+    values do not fit."""
+    _contig(c_kv, k_rope, prefix_len, status)
+    B, Tcap, _ = c_kv.shape
+    D = acc.accept_idx.shape[1] - 1
+    a = acc.c()
+    _check(lib().ddt_kv_commit(ctypes.byref(a), B, D, Tcap, _ptr(c_kv), _ptr(k_rope), _ptr(prefix_len),
+                               _ptr(status), _stream_ptr(stream)), "ddt_kv_commit")
 
 
 class VerifyStep:

@@ -51,6 +51,8 @@ def _load():
             lib.ddto_attn_rows.restype = i
             lib.ddto_tree_accept.argtypes = [i, i, i, P, P, P, P, P, P, P, P]
             lib.ddto_tree_accept.restype = i
+            lib.ddto_kv_commit.argtypes = [i, i, i, P, P, P, P, P, P]
+            lib.ddto_kv_commit.restype = i
             _lib = lib
     return _lib
 
@@ -137,3 +139,22 @@ def tree_accept(tree: Tree, target_argmax, D: int):
                          _p(r["accept_len"]), _p(r["accept_idx"]), _p(r["commit_tok"]),
                          _p(r["next_root"]))
     return r
+
+
+def kv_commit(accept_len, accept_idx, c_kv_bits, k_rope_bits, prefix_len, status, D: int):
+    """Moves the accepted path's keys into the committed prefix. Works on
+    copies: c_kv_bits [B,Tcap,512] and k_rope_bits [B,Tcap,64] as uint16 bf16
+    bit patterns, prefix_len and status int32 [B]. Returns the four new arrays
+    (c_kv, k_rope, prefix_len, status)."""
+    lib = _load()
+    kv = np.array(c_kv_bits, dtype=np.uint16, order="C", copy=True)
+    kr = np.array(k_rope_bits, dtype=np.uint16, order="C", copy=True)
+    B, Tcap, _ = kv.shape
+    pl = np.array(prefix_len, dtype=np.int32, copy=True)
+    st = np.array(status, dtype=np.int32, copy=True)
+    al = np.ascontiguousarray(accept_len, np.int32)
+    ai = np.ascontiguousarray(accept_idx, np.int32)
+    rc = lib.ddto_kv_commit(B, D, Tcap, _p(al), _p(ai), _p(kv), _p(kr), _p(pl), _p(st))
+    if rc != 0:
+        raise MemoryError("ddto_kv_commit: out of host memory")
+    return kv, kr, pl, st

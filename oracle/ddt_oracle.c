@@ -16,6 +16,12 @@
  *                   Thousand-Parameter Decision", "What to Build New", item 2;
  *                   "The Milestone Message", section "Architectural Abstraction":
  *                   the [ones | visibility] mask over positions L + depth).
+ *  ddto_kv_commit   moves the accepted nodes' latent and rotary keys into the
+ *                   committed prefix ("The Architecture of a Thousand-Parameter
+ *                   Decision", "What to Build New", items 4 and 5: the step
+ *                   ends with an append of the committed tokens' KV; node m's
+ *                   key at row T_b + m as in "The Milestone Message",
+ *                   "Architectural Abstraction").
  *  ddto_tree_accept greedy follow-the-verified-tree walk ("The Architecture of
  *                   Closure", the kernel table row for tree_accept.cu).
  *
@@ -325,5 +331,55 @@ int ddto_tree_accept(int B, int D, int Qc, const int32_t *token, const int32_t *
         accept_len[b] = len;
         next_root[b] = tg[cur];
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* KV commit                                                           */
+/* ------------------------------------------------------------------ */
+
+/* For each sequence b with T = prefix_len[b] and L = accept_len[b], the
+ * accepted path is nodes accept_idx[b][0..L-1] (node 0, the root, first).
+ * Node m's keys are rows T + m of c_kv (512 bf16 per row) and k_rope (64 bf16
+ * per row). After the commit the path's keys are rows T .. T + L - 1 in path
+ * order, rows below T are unchanged, and prefix_len[b] = T + L. A sequence
+ * whose values are out of range (L outside [1, D+1], T < 0, T + L > Tcap, a
+ * path index not increasing, or a node row at or past Tcap) is left
+ * unchanged and flagged BADINPUT in status[b]; others keep their status.
+ * Rows are 16-bit words copied as bytes. */
+int ddto_kv_commit(int B, int D, int Tcap, const int32_t *accept_len, const int32_t *accept_idx,
+                   uint16_t *c_kv, uint16_t *k_rope, int32_t *prefix_len, int32_t *status) {
+    uint16_t *tmp_kv = (uint16_t *)malloc(sizeof(uint16_t) * 512 * (size_t)(D + 1));
+    uint16_t *tmp_kr = (uint16_t *)malloc(sizeof(uint16_t) * 64 * (size_t)(D + 1));
+    if (!tmp_kv || !tmp_kr) {
+        free(tmp_kv);
+        free(tmp_kr);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        const int T = prefix_len[b], L = accept_len[b];
+        const int32_t *ai = accept_idx + (size_t)b * (D + 1);
+        int ok = L >= 1 && L <= D + 1 && T >= 0 && (long long)T + L <= Tcap && ai[0] == 0;
+        for (int k = 1; ok && k < L; ++k)
+            if (ai[k] <= ai[k - 1] || (long long)T + ai[k] >= Tcap) ok = 0;
+        if (!ok) {
+            status[b] = ORACLE_BADINPUT;
+            continue;
+        }
+        uint16_t *kv = c_kv + (size_t)b * Tcap * 512, *kr = k_rope + (size_t)b * Tcap * 64;
+        /* read every source row before writing any (a later source row can be
+         * an earlier destination) */
+        for (int k = 0; k < L; ++k) {
+            memcpy(tmp_kv + (size_t)k * 512, kv + (size_t)(T + ai[k]) * 512, sizeof(uint16_t) * 512);
+            memcpy(tmp_kr + (size_t)k * 64, kr + (size_t)(T + ai[k]) * 64, sizeof(uint16_t) * 64);
+        }
+        for (int k = 0; k < L; ++k) {
+            memcpy(kv + (size_t)(T + k) * 512, tmp_kv + (size_t)k * 512, sizeof(uint16_t) * 512);
+            memcpy(kr + (size_t)(T + k) * 64, tmp_kr + (size_t)k * 64, sizeof(uint16_t) * 64);
+        }
+        prefix_len[b] = T + L;
+    }
+    free(tmp_kv);
+    free(tmp_kr);
     return 0;
 }

@@ -107,3 +107,23 @@ def test_accept_rejects_null(L):
 def test_workspace_size_rejects_bad_shapes(L):
     assert L.ddt_workspace_size(0, 4, 4, 8, 4, 64) == 0
     assert L.ddt_workspace_size(1, 4, 4, 65, 4, 64) == 0
+
+
+def test_kv_commit_rejects_bad_arguments(L):
+    acc = ddtree.DdtAccept(FAKE, FAKE, FAKE, FAKE)
+    kv = 0x2000  # 16-byte aligned, never dereferenced
+    args = dict(B=2, D=8, Tcap=64, kv=kv, kr=kv, pl=FAKE, st=FAKE)
+
+    def call(acc_=acc, **kw):
+        a = dict(args, **kw)
+        return L.ddt_kv_commit(ctypes.byref(acc_) if acc_ is not None else None, a["B"], a["D"], a["Tcap"],
+                               a["kv"], a["kr"], a["pl"], a["st"], None)
+    assert call(acc_=None) == ddtree.DDT_E_INVAL
+    assert call(acc_=ddtree.DdtAccept(None, FAKE, FAKE, FAKE)) == ddtree.DDT_E_INVAL
+    assert call(B=0) == ddtree.DDT_E_INVAL
+    assert call(D=0) == ddtree.DDT_E_INVAL
+    assert call(D=17) == ddtree.DDT_E_INVAL
+    assert call(Tcap=0) == ddtree.DDT_E_INVAL
+    assert call(kv=kv + 2) == ddtree.DDT_E_INVAL
+    assert call(kr=None) == ddtree.DDT_E_INVAL
+    assert call(pl=None) == ddtree.DDT_E_INVAL
