@@ -367,6 +367,35 @@ def gpu_arm(args, wl_idx, rank, world, local_rank):
     roof["algorithmic_bytes_per_launch"] = algo_bytes
     roof["launch_ms"] = attn_ms
 
+    # ---- the same attention on a block-table (paged) cache: every key row in
+    # a shuffled pool with junk rows, gathered by the kernel
+    rng = np.random.default_rng(7)
+    n_pool = wl.B * inp.Tcap + 1024
+    perm = torch.from_numpy(rng.permutation(n_pool)[: wl.B * inp.Tcap].astype(np.int64)).to(dev)
+    pool_kv = torch.zeros(n_pool, 512, dtype=torch.bfloat16, device=dev)
+    pool_kr = torch.zeros(n_pool, 64, dtype=torch.bfloat16, device=dev)
+    pool_kv[perm] = c_kv.reshape(-1, 512)
+    pool_kr[perm] = k_rope.reshape(-1, 64)
+    kv_index = perm.to(torch.int32).reshape(wl.B, inp.Tcap).contiguous()
+    with torch.cuda.stream(s):
+        ddtree.ddt_verify_mla_attn_paged(q_lat, q_rope, pool_kv, pool_kr, pl, kv_index, step.tree, inp.scale,
+                                         attn_out, attn_lse, step.workspace, stream=s)
+    torch.cuda.synchronize()
+    gp = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gp, stream=s):
+        ddtree.ddt_verify_mla_attn_paged(q_lat, q_rope, pool_kv, pool_kr, pl, kv_index, step.tree, inp.scale,
+                                         attn_out, attn_lse, step.workspace, stream=s)
+    for _ in timed(gp, 3):
+        pass
+    torch.cuda.synchronize()
+    pevs = timed(gp, max(args.steps, 10))
+    torch.cuda.synchronize()
+    paged_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in pevs)
+    paged = {"us": paged_ms * 1e3, "tflops": flop / (paged_ms / 1e3) / 1e12,
+             "vs_contiguous": attn_ms / paged_ms, "pool_rows": n_pool,
+             "note": "block table of page size 1 over a shuffled pool; the producer warp gathers rows with cp.async"}
+    del pool_kv, pool_kr, kv_index, perm
+
     # ---- the KV commit after accept (the append of the accepted path's keys),
     # timed alone on scratch copies of the cache; the prefix lengths it
     # advances are reset before each call, outside the timed window
@@ -461,6 +490,7 @@ def gpu_arm(args, wl_idx, rank, world, local_rank):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "kv_commit": kv_commit,
+        "paged_attn": paged,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

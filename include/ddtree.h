@@ -169,6 +169,24 @@ int ddt_verify_step(const ddt_draft *draft, int budget, ddt_tree *tree,
                     const int32_t *target_argmax, ddt_accept *acc, void *workspace,
                     size_t ws_bytes, void *stream);
 
+/* Step 2 on a block-table (paged, page size 1) latent KV cache, the cache
+ * layout the pages use ("The Architecture of a Thousand-Parameter Decision:
+ * Designing a Native DDTree Inference Engine for Kimi K2.6", "What to Build
+ * New", item 5: a paged MLA-latent KV cache manager; "The Milestone Message",
+ * "Architectural Abstraction" for the positions). Same as ddt_verify_mla_attn
+ * except that in->c_kv and in->k_rope are pools of `pool_rows` rows
+ * ([pool_rows,512] and [pool_rows,64] bfloat16), and key position p of
+ * sequence b (prefix keys 0..T_b-1, node m at T_b + m) is pool row
+ * kv_index[b * in->Tcap + p]. kv_index is int32 [B, Tcap]; entries at and
+ * past a sequence's key end (T_b + n_nodes[b]) are not read for anything but
+ * may hold any value. An entry below the key end outside [0, pool_rows)
+ * flags the sequence DDT_E_BADINPUT (its rows are then undefined); host
+ * errors as for ddt_verify_mla_attn, plus DDT_E_INVAL for a null kv_index or
+ * pool_rows < 1. Workspace: ddt_workspace_size as for the contiguous cache. */
+int ddt_verify_mla_attn_paged(const ddt_attn_in *in, const ddt_tree *tree, float scale,
+                              ddt_attn_out *out, void *workspace, size_t ws_bytes,
+                              const int32_t *kv_index, int pool_rows, void *stream);
+
 /* After accept: the KV append of the committed tokens ("The Architecture of a
  * Thousand-Parameter Decision: Designing a Native DDTree Inference Engine for
  * Kimi K2.6", "What to Build New", items 4 and 5: the step ends

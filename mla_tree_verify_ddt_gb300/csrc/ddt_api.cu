@@ -129,6 +129,18 @@ int ddt_verify_mla_attn(const ddt_attn_in *in, const ddt_tree *tree, float scale
                                    static_cast<cudaStream_t>(stream));
 }
 
+int ddt_verify_mla_attn_paged(const ddt_attn_in *in, const ddt_tree *tree, float scale, ddt_attn_out *out,
+                              void *workspace, size_t ws_bytes, const int32_t *kv_index, int pool_rows,
+                              void *stream) {
+    if (!kv_index || pool_rows < 1) return DDT_E_INVAL;
+    if (int rc = check_attn(in, tree, out)) return rc;
+    if (int rc = check_device()) return rc;
+    const ddt::AttnPlan plan = ddt::plan_attention(tree->B, tree->Qc, in->H, in->Tcap, device_info()->sms);
+    if (plan.ws_bytes > ws_bytes || (plan.ws_bytes && !workspace)) return DDT_E_INVAL;
+    return ddt::launch_verify_attn(*in, *tree, scale, *out, workspace, ws_bytes, plan,
+                                   static_cast<cudaStream_t>(stream), false, kv_index, pool_rows);
+}
+
 int ddt_tree_accept(const ddt_tree *tree, const int32_t *target_argmax, ddt_accept *out, void *stream) {
     if (int rc = check_accept(tree, target_argmax, out)) return rc;
     if (int rc = check_device()) return rc;

@@ -125,8 +125,10 @@ enum {
     NUM_BARS = 28
 };
 
-// arrival count of barrier i (see the enum)
-__device__ __forceinline__ uint32_t bar_count(int i) {
+// arrival count of barrier i (see the enum); with a block-table cache the
+// ring is filled by the 64 lanes of two gather warps instead of TMA
+__device__ __forceinline__ uint32_t bar_count(int i, bool gathered) {
+    if (gathered && i >= BAR_RING_FULL && i < BAR_RING_FULL + kSlots) return 64;  // two gather warps
     if (i == BAR_QT_READY || (i >= BAR_P_FULL && i < BAR_P_FULL + kSPBufs)) return 8;  // one per softmax warp
     if (i == BAR_SX_EMPTY) return 2 * kRows;  // every partner softmax thread
     if (i >= BAR_MAXX && i < BAR_MAXX + 4) return 2;  // warps q and q+4
@@ -146,6 +148,13 @@ struct AttnArgs {
     size_t rows_total;       // B * Qc * H
     float scale_log2;        // scale * log2(e)
     unsigned long long wait_ns;
+    // block-table cache: key position p of sequence b is row kv_index[b*Tcap + p]
+    // of the pools c_kv [pool_rows][512] and k_rope [pool_rows][64]; null for
+    // the contiguous cache read by TMA
+    const int32_t *kv_index;
+    const uint8_t *pool_kv;
+    const uint8_t *pool_kr;
+    int pool_rows;
 };
 
 // Visibility of keys key0..key0+31 (half a tile) for a node with ancestor
@@ -230,7 +239,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // arrived on here (relaxed: the init fence already releases the inits);
     // the softmax threads wait on it just before their first remote store.
     if (warp == kProducerWarp) {
-        if (lane < NUM_BARS) mbar_init(bar(lane), bar_count(lane));
+        if (lane < NUM_BARS) mbar_init(bar(lane), bar_count(lane, a.kv_index != nullptr));
         if (lane == 0) *abort_flag = 0;
         mbar_fence_init();
         __syncwarp();
@@ -300,6 +309,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
 
 
+    // Block-table cache: each tile's 64 keys come from arbitrary pool rows.
+    // Two warps (the producer and, after its fetch, the tree warp; on
+    // different SM sub-partitions) each copy 32 of them, 16 bytes per lane,
+    // one key's contiguous half-row per instruction, into the same swizzled
+    // layout the tensor-map loads produce; each lane arrives on the slot's
+    // barrier once its copies have landed. Block-table entries are checked for
+    // keys below the sequence's key end (the tree is known first); a bad entry
+    // reads row 0 and flags the sequence; entries past the key end are not
+    // used for anything.
+    auto gather_keys = [&](int k_lo) {
+        grid_dep_wait();
+        const int n_g = a.n_nodes[b] < 1 ? 1 : (a.n_nodes[b] > a.Qc ? a.Qc : a.n_nodes[b]);
+        const int kend_g = (t_ok && static_cast<long long>(T) + n_g <= a.Tcap) ? T + n_g : 0;
+        const int32_t *kvi = a.kv_index + static_cast<size_t>(b) * a.Tcap;
+        bool ok = true, bad_index = false;
+        for (int jj = 0; jj < nrange; ++jj) {
+            const int slot = jj % kSlots, use = jj / kSlots;
+            if (use >= 1 &&
+                !__all_sync(0xffffffffu, mbar_wait(bar(BAR_RING_EMPTY + slot), (use - 1) & 1, deadline, abort_flag))) {
+                ok = false;
+                break;
+            }
+            const uint32_t dst = sRing + slot * kSlotBytes;
+            // pool row of key k_lo + lane of the tile
+            const int key = (t0 + jj) * kKeys + k_lo + lane;
+            int phys = key < a.Tcap ? kvi[key] : 0;
+            if (phys < 0 || phys >= a.pool_rows) {
+                if (key < kend_g) bad_index = true;
+                phys = 0;
+            }
+            // latent half-rows: lane l copies its 16 bytes (4 chunks x 8
+            // groups, 128-byte swizzle)
+#pragma unroll 4
+            for (int i = 0; i < 32; ++i) {
+                const int r = k_lo + i;
+                const int pr = __shfl_sync(0xffffffffu, phys, i);
+                cp_async_16(dst + (lane >> 3) * kChunkBytesKV + r * 128 + (((lane & 7) ^ (r & 7)) << 4),
+                            a.pool_kv + static_cast<size_t>(pr) * 1024 + rank * 512 + lane * 16);
+            }
+            // rotary rows: 8 keys per instruction, 4 lanes each (64-byte swizzle)
+#pragma unroll
+            for (int i0 = 0; i0 < 32; i0 += 8) {
+                const int i = i0 + (lane >> 2), q = lane & 3, r = k_lo + i;
+                const int pr = __shfl_sync(0xffffffffu, phys, i);
+                cp_async_16(dst + kQChunks * kChunkBytesKV + r * 64 + ((q ^ ((r >> 1) & 3)) << 4),
+                            a.pool_kr + static_cast<size_t>(pr) * 128 + rank * 64 + q * 16);
+            }
+            cp_async_arrive_noinc(bar(BAR_RING_FULL + slot));
+        }
+        if (!ok && lane == 0) fail();
+        if (__any_sync(0xffffffffu, bad_index) && lane == 0) a.status[b] = DDT_E_BADINPUT;
+        cp_async_wait_all();  // every copy has landed before the CTA can leave
+    };
+
     float *lse_out = nullptr;  // set by the softmax threads that write an lse
     float lse_val = 0.f;
     if (nrange <= 0) {
@@ -316,6 +379,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int zero = 0;
             mbar_wait(bar(BAR_Q_FULL), 0, globaltimer_ns() + 100000000ull, &zero);
         }
+    } else if (warp == kProducerWarp && a.kv_index) {
+        // ======================= KV gather, keys 0-31 of each tile =======================
+        gather_keys(0);
     } else if (warp == kProducerWarp) {
         // ======================= TMA producer =======================
         if (lane == 0) {
@@ -360,6 +426,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) *reinterpret_cast<volatile int *>(smem + kOffTree) = a.n_nodes[b];
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_TREE));
+        if (a.kv_index) gather_keys(32);  // ======== KV gather, keys 32-63 of each tile
     } else if (warp == kMmaWarp) {
         // ======================= MMA issuer =======================
         if (lane == 0) {
@@ -431,6 +498,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                // gathered tiles were written by ordinary (generic-proxy)
+                // copies: order them before the tensor core's reads
+                if (a.kv_index) fence_proxy_async_smem();
                 tc_fence_after();
                 const uint32_t dS = tmem + kColSP + sb * 64;
                 const uint32_t kb = sRing + slot * kSlotBytes;
@@ -893,11 +963,14 @@ AttnPlan plan_attention(int B, int Qc, int H, int Tcap, int sms) {
 
 int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
                        const ddt_attn_out &out, void *workspace, size_t ws_bytes,
-                       const AttnPlan &plan, cudaStream_t s, bool after_prev) {
+                       const AttnPlan &plan, cudaStream_t s, bool after_prev, const int32_t *kv_index,
+                       int pool_rows) {
     EncodeTiledFn enc = get_encoder();
     if (!enc) return DDT_E_CUDA;
     const uint64_t rows_total = static_cast<uint64_t>(tree.B) * tree.Qc * in.H;
-    const uint64_t kv_rows = static_cast<uint64_t>(tree.B) * in.Tcap;
+    // (with a block table the KV maps cover the pools; the gather path does
+    // not use them)
+    const uint64_t kv_rows = kv_index ? static_cast<uint64_t>(pool_rows) : static_cast<uint64_t>(tree.B) * in.Tcap;
     CUtensorMap tm_q, tm_kv, tm_kr;
     if (!encode_2d(enc, &tm_q, in.q_lat, 512, rows_total, 64, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(enc, &tm_kv, in.c_kv, 512, kv_rows, 64, kKeys, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -928,6 +1001,10 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
     a.rows_total = rows_total;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     a.wait_ns = kWaitLimitNs;
+    a.kv_index = kv_index;
+    a.pool_kv = static_cast<const uint8_t *>(in.c_kv);
+    a.pool_kr = static_cast<const uint8_t *>(in.k_rope);
+    a.pool_rows = pool_rows;
     float *ws_o = nullptr, *ws_lse = nullptr;
     if (plan.nsplit > 1) {
         if (!workspace || ws_bytes < plan.ws_bytes) return DDT_E_INVAL;

@@ -23,7 +23,8 @@ MAX_DEPTH, MAX_TOPK, MAX_BUDGET, LATENT, ROPE = 16, 16, 64, 512, 64
 
 EXPORTED = ["ddt_workspace_size", "ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept",
             "ddt_verify_step", "ddt_status_str", "ddt_read_device_status",
-            "ddt_selftest_bounded_wait", "ddt_verify_mla_attn_noalloc", "ddt_kv_commit"]
+            "ddt_selftest_bounded_wait", "ddt_verify_mla_attn_noalloc", "ddt_kv_commit",
+            "ddt_verify_mla_attn_paged"]
 
 P = ctypes.c_void_p
 I = ctypes.c_int
@@ -83,13 +84,15 @@ def lib() -> ctypes.CDLL:
         L.ddt_verify_mla_attn_noalloc.argtypes = [ctypes.POINTER(DdtAttnIn), ctypes.POINTER(DdtTree),
                                                   ctypes.c_float, ctypes.POINTER(DdtAttnOut), P]
         L.ddt_kv_commit.argtypes = [ctypes.POINTER(DdtAccept), I, I, I, P, P, P, P, P]
+        L.ddt_verify_mla_attn_paged.argtypes = [ctypes.POINTER(DdtAttnIn), ctypes.POINTER(DdtTree), ctypes.c_float,
+                                                ctypes.POINTER(DdtAttnOut), P, ctypes.c_size_t, P, I, P]
         L.ddt_status_str.argtypes = [I]
         L.ddt_status_str.restype = ctypes.c_char_p
         L.ddt_read_device_status.argtypes = [P, I, P]
         L.ddt_selftest_bounded_wait.argtypes = [P, ctypes.c_uint, P]
         for f in ("ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept", "ddt_verify_step",
                   "ddt_read_device_status", "ddt_selftest_bounded_wait",
-                  "ddt_verify_mla_attn_noalloc", "ddt_kv_commit"):
+                  "ddt_verify_mla_attn_noalloc", "ddt_kv_commit", "ddt_verify_mla_attn_paged"):
             getattr(L, f).restype = I
         _lib = L
     return _lib
@@ -220,6 +223,31 @@ def ddt_verify_mla_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: Tree, sca
     _check(lib().ddt_verify_mla_attn(ctypes.byref(a), ctypes.byref(t), float(scale),
                                      ctypes.byref(o), _ptr(workspace), wsb, _stream_ptr(stream)),
            "ddt_verify_mla_attn")
+    return out, lse
+
+
+def ddt_verify_mla_attn_paged(q_lat, q_rope, pool_kv, pool_kr, prefix_len, kv_index, tree: Tree, scale: float,
+                              out=None, lse=None, workspace=None, stream=None):
+    """Attention on a block-table cache: key position p of sequence b is row
+    kv_index[b, p] of pool_kv [P,512] / pool_kr [P,64] (bf16); kv_index is
+    int32 [B, Tcap]."""
+    _contig(q_lat, q_rope, pool_kv, pool_kr, prefix_len, kv_index)
+    B, Qc, H, _ = q_lat.shape
+    Tcap = kv_index.shape[1]
+    if out is None:
+        out = torch.empty(B, Qc, H, LATENT, dtype=torch.float32, device=q_lat.device)
+    if lse is None:
+        lse = torch.empty(B, Qc, H, dtype=torch.float32, device=q_lat.device)
+    ws = ddt_workspace_size(B, tree.D, 1, Qc - 1, H, Tcap)
+    if workspace is None and ws:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=q_lat.device)
+    a = DdtAttnIn(H, Tcap, _ptr(q_lat), _ptr(q_rope), _ptr(pool_kv), _ptr(pool_kr), _ptr(prefix_len))
+    o = DdtAttnOut(_ptr(out), _ptr(lse))
+    t = tree.c()
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().ddt_verify_mla_attn_paged(ctypes.byref(a), ctypes.byref(t), float(scale), ctypes.byref(o),
+                                           _ptr(workspace), wsb, _ptr(kv_index), pool_kv.shape[0],
+                                           _stream_ptr(stream)), "ddt_verify_mla_attn_paged")
     return out, lse
 
 

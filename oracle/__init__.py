@@ -158,3 +158,18 @@ def kv_commit(accept_len, accept_idx, c_kv_bits, k_rope_bits, prefix_len, status
     if rc != 0:
         raise MemoryError("ddto_kv_commit: out of host memory")
     return kv, kr, pl, st
+
+
+def gather_paged(pool_kv, pool_kr, kv_index):
+    """The contiguous cache a block-table cache stands for: row p of sequence
+    b is pool row kv_index[b, p]. Entries outside [0, P) give zero rows (such
+    positions must not be visible to any node)."""
+    kvi = np.asarray(kv_index)
+    P = pool_kv.shape[0]
+    ok = (kvi >= 0) & (kvi < P)
+    idx = np.where(ok, kvi, 0)
+    kv = np.asarray(pool_kv)[idx]
+    kr = np.asarray(pool_kr)[idx]
+    kv[~ok] = 0
+    kr[~ok] = 0
+    return kv, kr

@@ -127,3 +127,13 @@ def test_kv_commit_rejects_bad_arguments(L):
     assert call(kv=kv + 2) == ddtree.DDT_E_INVAL
     assert call(kr=None) == ddtree.DDT_E_INVAL
     assert call(pl=None) == ddtree.DDT_E_INVAL
+
+
+def test_paged_attention_rejects_missing_block_table(L):
+    a = ddtree.DdtAttnIn(4, 64, FAKE, FAKE, FAKE, FAKE, FAKE)
+    t = _tree()
+    o = ddtree.DdtAttnOut(FAKE, FAKE)
+    assert L.ddt_verify_mla_attn_paged(ctypes.byref(a), ctypes.byref(t), ctypes.c_float(0.1), ctypes.byref(o),
+                                       None, 0, None, 8, None) == ddtree.DDT_E_INVAL
+    assert L.ddt_verify_mla_attn_paged(ctypes.byref(a), ctypes.byref(t), ctypes.c_float(0.1), ctypes.byref(o),
+                                       None, 0, FAKE, 0, None) == ddtree.DDT_E_INVAL
