@@ -367,6 +367,26 @@ def gpu_arm(args, wl_idx, rank, world, local_rank):
     roof["algorithmic_bytes_per_launch"] = algo_bytes
     roof["launch_ms"] = attn_ms
 
+    # ---- the same attention with the latent output in bfloat16
+    out16 = torch.empty(attn_out.shape, dtype=torch.bfloat16, device=dev)
+    with torch.cuda.stream(s):
+        ddtree.ddt_verify_mla_attn_bf16(q_lat, q_rope, c_kv, k_rope, pl, step.tree, inp.scale, out16, attn_lse,
+                                        step.workspace, stream=s)
+    torch.cuda.synchronize()
+    gb = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gb, stream=s):
+        ddtree.ddt_verify_mla_attn_bf16(q_lat, q_rope, c_kv, k_rope, pl, step.tree, inp.scale, out16, attn_lse,
+                                        step.workspace, stream=s)
+    for _ in timed(gb, 3):
+        pass
+    torch.cuda.synchronize()
+    bevs = timed(gb, max(args.steps, 10))
+    torch.cuda.synchronize()
+    bf16_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in bevs)
+    bf16_out = {"us": bf16_ms * 1e3, "tflops": flop / (bf16_ms / 1e3) / 1e12, "vs_float32_out": attn_ms / bf16_ms,
+                "out_bytes": int(out16.numel()) * 2}
+    del out16
+
     # ---- the same attention on a block-table (paged) cache: every key row in
     # a shuffled pool with junk rows, gathered by the kernel
     rng = np.random.default_rng(7)
@@ -491,6 +511,7 @@ def gpu_arm(args, wl_idx, rank, world, local_rank):
         "gpu_launches": launches_per_step * args.steps,
         "kv_commit": kv_commit,
         "paged_attn": paged,
+        "bf16_out_attn": bf16_out,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

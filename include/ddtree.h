@@ -169,6 +169,15 @@ int ddt_verify_step(const ddt_draft *draft, int budget, ddt_tree *tree,
                     const int32_t *target_argmax, ddt_accept *acc, void *workspace,
                     size_t ws_bytes, void *stream);
 
+/* Step 2 with the latent output in bfloat16, the type the absorbed-MLA
+ * value up-projection that follows it takes ("The Milestone Message",
+ * section "MLA": the absorb form with w_kc / w_vc). Same as
+ * ddt_verify_mla_attn, except that out_bf16 [B,Qc,H,512] (16-byte aligned)
+ * receives each output element rounded to nearest even from its float32
+ * value; lse stays float32 [B,Qc,H]. Same workspace and errors. */
+int ddt_verify_mla_attn_bf16(const ddt_attn_in *in, const ddt_tree *tree, float scale, uint16_t *out_bf16,
+                             float *lse, void *workspace, size_t ws_bytes, void *stream);
+
 /* Step 2 on a block-table (paged, page size 1) latent KV cache, the cache
  * layout the pages use ("The Architecture of a Thousand-Parameter Decision:
  * Designing a Native DDTree Inference Engine for Kimi K2.6", "What to Build

@@ -129,6 +129,19 @@ int ddt_verify_mla_attn(const ddt_attn_in *in, const ddt_tree *tree, float scale
                                    static_cast<cudaStream_t>(stream));
 }
 
+int ddt_verify_mla_attn_bf16(const ddt_attn_in *in, const ddt_tree *tree, float scale, uint16_t *out_bf16,
+                             float *lse, void *workspace, size_t ws_bytes, void *stream) {
+    // (the float32 output slot carries the bfloat16 buffer; check_attn tests
+    // its pointer and alignment)
+    ddt_attn_out out{reinterpret_cast<float *>(out_bf16), lse};
+    if (int rc = check_attn(in, tree, &out)) return rc;
+    if (int rc = check_device()) return rc;
+    const ddt::AttnPlan plan = ddt::plan_attention(tree->B, tree->Qc, in->H, in->Tcap, device_info()->sms);
+    if (plan.ws_bytes > ws_bytes || (plan.ws_bytes && !workspace)) return DDT_E_INVAL;
+    return ddt::launch_verify_attn(*in, *tree, scale, out, workspace, ws_bytes, plan,
+                                   static_cast<cudaStream_t>(stream), false, nullptr, 0, true);
+}
+
 int ddt_verify_mla_attn_paged(const ddt_attn_in *in, const ddt_tree *tree, float scale, ddt_attn_out *out,
                               void *workspace, size_t ws_bytes, const int32_t *kv_index, int pool_rows,
                               void *stream) {

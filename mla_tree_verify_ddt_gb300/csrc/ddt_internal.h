@@ -35,7 +35,7 @@ AttnPlan plan_attention(int B, int Qc, int H, int Tcap, int sms);
 int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
                        const ddt_attn_out &out, void *workspace, size_t ws_bytes,
                        const AttnPlan &plan, cudaStream_t s, bool after_prev = false,
-                       const int32_t *kv_index = nullptr, int pool_rows = 0);
+                       const int32_t *kv_index = nullptr, int pool_rows = 0, bool out_bf16 = false);
 
 // cudaLaunchKernelEx with the programmatic-stream-serialization attribute
 // when `after_prev`, a plain launch otherwise.

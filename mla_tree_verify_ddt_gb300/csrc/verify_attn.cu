@@ -155,6 +155,9 @@ struct AttnArgs {
     const uint8_t *pool_kv;
     const uint8_t *pool_kr;
     int pool_rows;
+    // the output is stored as bfloat16 (only when the key range is not split;
+    // split partials stay float32 and the merge kernel rounds)
+    int out_bf16;
 };
 
 // Visibility of keys key0..key0+31 (half a tile) for a node with ancestor
@@ -177,6 +180,55 @@ __device__ __noinline__ uint32_t half_tile_visibility(int key0, int T, int n, ui
         vis |= static_cast<uint32_t>(v) << k;
     }
     return vis;
+}
+
+// The epilogue's staging of one thread's 128 output columns (tensor-memory
+// columns o_col .. o_col+127 of its lane, times inv_l, or zeros) in the KV
+// ring as the boxes the tensor store reads: four 128-row x 32-column float32
+// boxes, or two 128-row x 64-column bfloat16 boxes (rounded to nearest even),
+// in the 128-byte swizzle (16-byte group j of row r at j ^ (r % 8)). Written
+// this way each warp store is conflict-free, where direct row-strided global
+// stores cost a transaction per lane. Out of line, so its temporaries do not
+// weigh on the register allocation of the kernel's main loop.
+__device__ __noinline__ void stage_output(uint32_t o_col, uint8_t *ring, int half, int row, bool zero_row,
+                                          float inv_l, bool bf16) {
+    if (!bf16) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_col + c * 32, o);
+            tmem_wait_ld();
+            uint8_t *box_row = ring + (half * 4 + c) * kOutBoxBytes + row * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 v = zero_row ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                          : make_float4(__uint_as_float(o[4 * j]) * inv_l,
+                                                        __uint_as_float(o[4 * j + 1]) * inv_l,
+                                                        __uint_as_float(o[4 * j + 2]) * inv_l,
+                                                        __uint_as_float(o[4 * j + 3]) * inv_l);
+                *reinterpret_cast<float4 *>(box_row + ((j ^ (row & 7)) << 4)) = v;
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(o_col + cc * 32, o);
+            tmem_wait_ld();
+            uint8_t *box_row = ring + (half * 2 + (cc >> 1)) * kOutBoxBytes + row * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t w[4];
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    w[v] = zero_row ? 0u
+                                    : pack_bf16x2(__uint_as_float(o[8 * j + 2 * v]) * inv_l,
+                                                  __uint_as_float(o[8 * j + 2 * v + 1]) * inv_l);
+                const int grp = (cc & 1) * 4 + j;
+                *reinterpret_cast<uint4 *>(box_row + ((grp ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -367,12 +419,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float lse_val = 0.f;
     if (nrange <= 0) {
         // nothing visible in this range: zero rows (this CTA's half), lse = -inf
-        for (int idx = tid; idx < kRows * 64; idx += kThreads) {
-            const int r = idx >> 6, c4 = idx & 63;
+        // (this CTA's 256 columns of a row: 64 float4, or 32 uint4 of bfloat16)
+        const int per_row = a.out_bf16 ? 32 : 64;
+        for (int idx = tid; idx < kRows * per_row; idx += kThreads) {
+            const int r = idx / per_row, c4 = idx % per_row;
             const int g = mt * kRows + r;
             if (g >= rows_seq) continue;
-            float4 *dst = reinterpret_cast<float4 *>(o_dst + (row_base + g) * 512 + rank * 256) + c4;
-            *dst = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (a.out_bf16)
+                reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(o_dst) + (row_base + g) * 512 + rank * 256)[c4] =
+                    make_uint4(0u, 0u, 0u, 0u);
+            else
+                reinterpret_cast<float4 *>(o_dst + (row_base + g) * 512 + rank * 256)[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (rank == 0 && c4 == 0) lse_dst[row_base + g] = -INFINITY;
         }
         if (warp == kProducerWarp && lane == 0) {
@@ -772,28 +829,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // this sequence's keys, are zero (tensor memory was not written)
             const bool zero_row = !node_ok;
             const float inv_l = (l_sum > 0.f && !zero_row) ? 1.0f / l_sum : 0.f;
-            // Stage this thread's 128 output columns in the KV ring (idle once
-            // every PV is done) as four of the eight 128-row x 32-column fp32
-            // boxes of this CTA's half, in the 128-byte swizzle (16-byte chunk
-            // j of row r at chunk j ^ (r % 8)) that the tensor store reads.
-            // Written this way each warp store is conflict-free, where direct
-            // row-strided global stores cost a transaction per lane.
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_base + kColO + half * 128 + c * 32, o);
-                tmem_wait_ld();
-                uint8_t *box_row = smem + kOffRing + (half * 4 + c) * kOutBoxBytes + row * 128;
-                if (zero_row) {
-#pragma unroll
-                    for (int v = 0; v < 32; ++v) o[v] = 0u;
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<float4 *>(box_row + ((j ^ (row & 7)) << 4)) =
-                        make_float4(__uint_as_float(o[4 * j]) * inv_l, __uint_as_float(o[4 * j + 1]) * inv_l,
-                                    __uint_as_float(o[4 * j + 2]) * inv_l, __uint_as_float(o[4 * j + 3]) * inv_l);
-            }
+            // stage this thread's 128 output columns in the KV ring (idle
+            // once every PV is done) for the tensor store
+            stage_output(tmem + lane_base + kColO + half * 128, smem + kOffRing, half, row, zero_row, inv_l,
+                         a.out_bf16 != 0);
             fence_proxy_async_smem();
             // both CTAs hold the same row sum and max; one writes the lse
             // (after the final cluster barrier, like the output block)
@@ -829,8 +868,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncthreads();
     const bool store_out = tid == 0 && nrange > 0 && !*abort_flag;
     if (store_out) {
-        for (int c = 0; c < 8; ++c)
-            tma_store_3d(&tm_o, sRing + c * kOutBoxBytes, static_cast<int>(rank) * 256 + c * 32, mt * kRows,
+        // eight float32 boxes of 32 columns, or four bfloat16 boxes of 64
+        const int nbox = a.out_bf16 ? 4 : 8, box_cols = a.out_bf16 ? 64 : 32;
+        for (int c = 0; c < nbox; ++c)
+            tma_store_3d(&tm_o, sRing + c * kOutBoxBytes, static_cast<int>(rank) * 256 + c * box_cols, mt * kRows,
                          b + a.B * chunk);
         bulk_commit_group();
     }
@@ -850,7 +891,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // out = sum_c exp(lse_c - lse) out_c. One 128-thread block per row.
 __global__ void __launch_bounds__(128)
     merge_chunks_kernel(size_t rows_total, int nsplit, const float *__restrict__ ws_o,
-                        const float *__restrict__ ws_lse, float *__restrict__ out,
+                        const float *__restrict__ ws_lse, void *__restrict__ out, int out_bf16,
                         float *__restrict__ lse) {
     // the accept may start now; the partials are complete once the
     // attention grid is
@@ -880,7 +921,11 @@ __global__ void __launch_bounds__(128)
         acc.z *= inv;
         acc.w *= inv;
     }
-    reinterpret_cast<float4 *>(out + r * 512)[threadIdx.x] = acc;
+    if (out_bf16)
+        reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + r * 512)[threadIdx.x] =
+            make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    else
+        reinterpret_cast<float4 *>(static_cast<float *>(out) + r * 512)[threadIdx.x] = acc;
     if (threadIdx.x == 0) lse[r] = (mx == -INFINITY) ? -INFINITY : mx + __logf(sum);
 }
 
@@ -918,13 +963,16 @@ bool encode_2d(EncodeTiledFn enc, CUtensorMap *m, const void *ptr, uint64_t cols
 
 // fp32 tensor [dim2][dim1][cols] row-major, box [box_rows, 32 columns] (128 bytes,
 // 128-byte swizzle), for tile stores
-bool encode_3d_f32_store(EncodeTiledFn enc, CUtensorMap *m, void *ptr, uint64_t cols, uint64_t dim1,
-                         uint64_t dim2, uint32_t box_rows) {
+// (or bfloat16 with 64-column boxes: 128 bytes either way)
+bool encode_3d_store(EncodeTiledFn enc, CUtensorMap *m, void *ptr, uint64_t cols, uint64_t dim1, uint64_t dim2,
+                     uint32_t box_rows, bool bf16) {
+    const uint64_t es = bf16 ? 2 : 4;
     cuuint64_t dims[3] = {cols, dim1, dim2};
-    cuuint64_t strides[2] = {cols * 4, dim1 * cols * 4};
-    cuuint32_t box[3] = {32, box_rows, 1};
+    cuuint64_t strides[2] = {cols * es, dim1 * cols * es};
+    cuuint32_t box[3] = {bf16 ? 64u : 32u, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -964,7 +1012,7 @@ AttnPlan plan_attention(int B, int Qc, int H, int Tcap, int sms) {
 int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
                        const ddt_attn_out &out, void *workspace, size_t ws_bytes,
                        const AttnPlan &plan, cudaStream_t s, bool after_prev, const int32_t *kv_index,
-                       int pool_rows) {
+                       int pool_rows, bool out_bf16) {
     EncodeTiledFn enc = get_encoder();
     if (!enc) return DDT_E_CUDA;
     const uint64_t rows_total = static_cast<uint64_t>(tree.B) * tree.Qc * in.H;
@@ -1017,9 +1065,10 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
         a.lse_dst = out.lse;
     }
     // the output (or the key-range partials) as [splits x B][Qc*H rows][512]
+    a.out_bf16 = (out_bf16 && plan.nsplit == 1) ? 1 : 0;
     CUtensorMap tm_o;
-    if (!encode_3d_f32_store(enc, &tm_o, a.o_dst, 512, static_cast<uint64_t>(tree.Qc) * in.H,
-                             static_cast<uint64_t>(tree.B) * plan.nsplit, kRows))
+    if (!encode_3d_store(enc, &tm_o, a.o_dst, 512, static_cast<uint64_t>(tree.Qc) * in.H,
+                         static_cast<uint64_t>(tree.B) * plan.nsplit, kRows, a.out_bf16 != 0))
         return DDT_E_INVAL;
     dim3 grid(plan.mtiles * 2, plan.nsplit, tree.B);
     if (launch_kernel(verify_attn_kernel, grid, dim3(kThreads), kSmemBytes, s, after_prev, tm_q, tm_kv, tm_kr, tm_o,
@@ -1028,7 +1077,8 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
     if (plan.nsplit > 1) {
         if (launch_kernel(merge_chunks_kernel, dim3(static_cast<unsigned>(rows_total)), dim3(128), 0, s, after_prev,
                           static_cast<size_t>(rows_total), plan.nsplit, static_cast<const float *>(ws_o),
-                          static_cast<const float *>(ws_lse), out.out, out.lse) != cudaSuccess)
+                          static_cast<const float *>(ws_lse), static_cast<void *>(out.out), out_bf16 ? 1 : 0,
+                          out.lse) != cudaSuccess)
             return DDT_E_CUDA;
     }
     return DDT_OK;

@@ -24,7 +24,7 @@ MAX_DEPTH, MAX_TOPK, MAX_BUDGET, LATENT, ROPE = 16, 16, 64, 512, 64
 EXPORTED = ["ddt_workspace_size", "ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept",
             "ddt_verify_step", "ddt_status_str", "ddt_read_device_status",
             "ddt_selftest_bounded_wait", "ddt_verify_mla_attn_noalloc", "ddt_kv_commit",
-            "ddt_verify_mla_attn_paged"]
+            "ddt_verify_mla_attn_paged", "ddt_verify_mla_attn_bf16"]
 
 P = ctypes.c_void_p
 I = ctypes.c_int
@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.ddt_verify_mla_attn_noalloc.argtypes = [ctypes.POINTER(DdtAttnIn), ctypes.POINTER(DdtTree),
                                                   ctypes.c_float, ctypes.POINTER(DdtAttnOut), P]
         L.ddt_kv_commit.argtypes = [ctypes.POINTER(DdtAccept), I, I, I, P, P, P, P, P]
+        L.ddt_verify_mla_attn_bf16.argtypes = [ctypes.POINTER(DdtAttnIn), ctypes.POINTER(DdtTree), ctypes.c_float,
+                                               P, P, P, ctypes.c_size_t, P]
         L.ddt_verify_mla_attn_paged.argtypes = [ctypes.POINTER(DdtAttnIn), ctypes.POINTER(DdtTree), ctypes.c_float,
                                                 ctypes.POINTER(DdtAttnOut), P, ctypes.c_size_t, P, I, P]
         L.ddt_status_str.argtypes = [I]
@@ -92,7 +94,8 @@ def lib() -> ctypes.CDLL:
         L.ddt_selftest_bounded_wait.argtypes = [P, ctypes.c_uint, P]
         for f in ("ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept", "ddt_verify_step",
                   "ddt_read_device_status", "ddt_selftest_bounded_wait",
-                  "ddt_verify_mla_attn_noalloc", "ddt_kv_commit", "ddt_verify_mla_attn_paged"):
+                  "ddt_verify_mla_attn_noalloc", "ddt_kv_commit", "ddt_verify_mla_attn_paged",
+                  "ddt_verify_mla_attn_bf16"):
             getattr(L, f).restype = I
         _lib = L
     return _lib
@@ -223,6 +226,26 @@ def ddt_verify_mla_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: Tree, sca
     _check(lib().ddt_verify_mla_attn(ctypes.byref(a), ctypes.byref(t), float(scale),
                                      ctypes.byref(o), _ptr(workspace), wsb, _stream_ptr(stream)),
            "ddt_verify_mla_attn")
+    return out, lse
+
+
+def ddt_verify_mla_attn_bf16(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: Tree, scale: float,
+                             out=None, lse=None, workspace=None, stream=None):
+    """ddt_verify_mla_attn with the latent output in bfloat16."""
+    _contig(q_lat, q_rope, c_kv, k_rope, prefix_len)
+    B, Qc, H, _ = q_lat.shape
+    if out is None:
+        out = torch.empty(B, Qc, H, LATENT, dtype=torch.bfloat16, device=q_lat.device)
+    if lse is None:
+        lse = torch.empty(B, Qc, H, dtype=torch.float32, device=q_lat.device)
+    ws = ddt_workspace_size(B, tree.D, 1, Qc - 1, H, c_kv.shape[1])
+    if workspace is None and ws:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=q_lat.device)
+    a = attn_in_struct(q_lat, q_rope, c_kv, k_rope, prefix_len)
+    t = tree.c()
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().ddt_verify_mla_attn_bf16(ctypes.byref(a), ctypes.byref(t), float(scale), _ptr(out), _ptr(lse),
+                                          _ptr(workspace), wsb, _stream_ptr(stream)), "ddt_verify_mla_attn_bf16")
     return out, lse
 
 
