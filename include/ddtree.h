@@ -214,6 +214,48 @@ int ddt_verify_mla_attn_paged(const ddt_attn_in *in, const ddt_tree *tree, float
 int ddt_kv_commit(const ddt_accept *acc, int B, int D, int Tcap, void *c_kv, void *k_rope,
                   int32_t *prefix_len, int32_t *status, void *stream);
 
+/* Temperature sampling at every tree node, the sampling commit path ("The
+ * Architecture of a Thousand-Parameter Decision: Designing a Native DDTree
+ * Inference Engine for Kimi K2.6", section "What to Reuse", item 3:
+ * temperature-based sampling from the verified token distribution; section
+ * "What to Build New", item 2: the sampling-probability path that normalises
+ * the target's probabilities over the tree nodes, and item 5: greedy and
+ * temperature commit paths).
+ *
+ * logits is float32 [B, tree->Qc, vocab] (16-byte aligned): row (b, i) holds
+ * the target's logits after node i. Its distribution is
+ * p_j = exp((x_j - M) / temperature) / S, M the row's largest logit. With
+ * u = u01[b, i] (float32 [B, Qc]) the node's sample is the first token id j
+ * with p_j > 0 whose cumulative probability p_0 + ... + p_j exceeds u; when
+ * none does (u >= 1, NaN, or rounding at the top) the last token with
+ * p_j > 0. temperature <= 0 selects the greedy limit: the first index of the
+ * largest logit (u01 is then not read and may be NULL).
+ *
+ *   sample_tok int32 [B, Qc]: the sample after each node; -1 for node slots
+ *              at or past n_nodes[b] and for rows with no distribution.
+ *   node_p     float32 [B, Qc]: node c's token's probability under its
+ *              parent's row (1 or 0 in the greedy limit); node 0 gets 1,
+ *              slots at or past n_nodes[b] get 0.
+ *
+ * Passing sample_tok to ddt_tree_accept as its target commits, at every
+ * accepted node, a token distributed as p (lossless tree sampling with a
+ * deterministic draft tree). Arithmetic: weights 2^((x - M) log2(e) / T)
+ * in float32 (hardware exp2, weights below 2^-126 of the largest flush to
+ * zero), sums in float32 up to 20480 tokens and float64 above; node_p is
+ * the child token's weight over the row total in float32. Cumulative
+ * probabilities are off by at most ~1e-5 of the total (worst case), so a
+ * sample can differ from exact arithmetic's only for u that close to a
+ * token boundary. A row holding a NaN, or (temperature > 0)
+ * whose largest logit is +-inf, gets sample -1, children's node_p 0 and
+ * DDT_E_BADINPUT in tree->status[b]; so does a child token outside
+ * [0, vocab). Host errors: DDT_E_INVAL for a null pointer, vocab < 4 or not
+ * a multiple of 4 or above 393216 (196608 on a device without 16-CTA
+ * clusters), misaligned logits, a NaN or infinite temperature, a positive
+ * temperature below 1e-30, or tree shape out of range. Reads tree->token,
+ * tree->parent, tree->n_nodes; allocates nothing. */
+int ddt_tree_sample(const ddt_tree *tree, const float *logits, int vocab, float temperature,
+                    const float *u01, int32_t *sample_tok, float *node_p, void *stream);
+
 /* Bytes of device scratch held by ddt_verify_mla_attn_noalloc (64 MiB). */
 #define DDT_NOALLOC_SCRATCH_BYTES (64u << 20)
 

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libddtree.so")
 SOURCES = ["ddt_api.cu", "tree_build.cu", "tree_accept.cu", "verify_attn.cu", "verify_attn_noalloc.cu",
-           "kv_commit.cu"]
+           "kv_commit.cu", "tree_sample.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

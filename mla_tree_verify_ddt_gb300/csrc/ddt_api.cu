@@ -3,6 +3,7 @@
 // the device except ddt_read_device_status.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 
 #include "ddt_internal.h"
@@ -192,6 +193,27 @@ int ddt_kv_commit(const ddt_accept *acc, int B, int D, int Tcap, void *c_kv, voi
     if (int rc = check_device()) return rc;
     return ddt::launch_kv_commit(B, D, Tcap, acc->accept_len, acc->accept_idx, c_kv, k_rope, prefix_len, status,
                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DDT_OK
+               : DDT_E_CUDA;
+}
+
+int ddt_tree_sample(const ddt_tree *tree, const float *logits, int vocab, float temperature, const float *u01,
+                    int32_t *sample_tok, float *node_p, void *stream) {
+    if (!tree || !logits || !sample_tok || !node_p) return DDT_E_INVAL;
+    if (!tree->token || !tree->parent || !tree->n_nodes || !tree->status) return DDT_E_INVAL;
+    if (tree->B < 1 || tree->Qc < 1 || tree->Qc > DDT_MAX_BUDGET + 1) return DDT_E_INVAL;
+    if (!(temperature == temperature) || temperature == INFINITY || temperature == -INFINITY) return DDT_E_INVAL;
+    if (temperature > 0.f && (temperature < 1e-30f || !u01)) return DDT_E_INVAL;
+    if (vocab < 4 || (vocab & 3) || !aligned16(logits)) return DDT_E_INVAL;
+    if (int rc = check_device()) return rc;
+    const int max_c = ddt::sample_max_cluster();
+    if (max_c == 0) return DDT_E_CUDA;
+    const ddt::SamplePlan plan =
+        ddt::plan_sample(vocab, static_cast<long long>(tree->B) * tree->Qc, device_info()->sms, max_c);
+    if (plan.C == 0) return DDT_E_INVAL;
+    const double kd = temperature > 0.f ? 1.4426950408889634 / static_cast<double>(temperature) : 0.0;
+    return ddt::launch_tree_sample(*tree, logits, vocab, kd, u01, sample_tok, node_p, plan,
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? DDT_OK
                : DDT_E_CUDA;
 }

@@ -60,6 +60,23 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 cudaError_t launch_kv_commit(int B, int D, int Tcap, const int32_t *accept_len, const int32_t *accept_idx,
                              void *c_kv, void *k_rope, int32_t *prefix_len, int32_t *status, cudaStream_t s);
 
+// Temperature sampling at every tree node: C CTAs (one cluster) per row of
+// logits, each holding 1024 * r tokens (r <= kSampleMaxRows).
+constexpr int kSampleMaxRows = 24;
+struct SamplePlan {
+    int C;        // CTAs per row (cluster size); 0 = shape not supported
+    int r;        // 128-token rows per warp region
+    size_t smem;  // dynamic shared memory per CTA
+};
+SamplePlan plan_sample(int V, long long rows, int sms, int max_cluster);
+// Largest cluster the sampling kernel may use on the current device (16 or
+// 8; 0 if its attributes could not be set). Sets the kernel's attributes on
+// the first call.
+int sample_max_cluster();
+// kd = log2(e) / temperature, or 0 for the greedy limit.
+cudaError_t launch_tree_sample(const ddt_tree &tree, const float *logits, int V, double kd, const float *u01,
+                               int32_t *sample_tok, float *node_p, const SamplePlan &plan, cudaStream_t s);
+
 cudaError_t launch_selftest_wait(int32_t *status, unsigned timeout_us, cudaStream_t s);
 
 }  // namespace ddt

@@ -24,7 +24,7 @@ MAX_DEPTH, MAX_TOPK, MAX_BUDGET, LATENT, ROPE = 16, 16, 64, 512, 64
 EXPORTED = ["ddt_workspace_size", "ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept",
             "ddt_verify_step", "ddt_status_str", "ddt_read_device_status",
             "ddt_selftest_bounded_wait", "ddt_verify_mla_attn_noalloc", "ddt_kv_commit",
-            "ddt_verify_mla_attn_paged", "ddt_verify_mla_attn_bf16"]
+            "ddt_verify_mla_attn_paged", "ddt_verify_mla_attn_bf16", "ddt_tree_sample"]
 
 P = ctypes.c_void_p
 I = ctypes.c_int
@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
                                                P, P, P, ctypes.c_size_t, P]
         L.ddt_verify_mla_attn_paged.argtypes = [ctypes.POINTER(DdtAttnIn), ctypes.POINTER(DdtTree), ctypes.c_float,
                                                 ctypes.POINTER(DdtAttnOut), P, ctypes.c_size_t, P, I, P]
+        L.ddt_tree_sample.argtypes = [ctypes.POINTER(DdtTree), P, I, ctypes.c_float, P, P, P, P]
         L.ddt_status_str.argtypes = [I]
         L.ddt_status_str.restype = ctypes.c_char_p
         L.ddt_read_device_status.argtypes = [P, I, P]
@@ -95,7 +96,7 @@ def lib() -> ctypes.CDLL:
         for f in ("ddt_tree_build", "ddt_verify_mla_attn", "ddt_tree_accept", "ddt_verify_step",
                   "ddt_read_device_status", "ddt_selftest_bounded_wait",
                   "ddt_verify_mla_attn_noalloc", "ddt_kv_commit", "ddt_verify_mla_attn_paged",
-                  "ddt_verify_mla_attn_bf16"):
+                  "ddt_verify_mla_attn_bf16", "ddt_tree_sample"):
             getattr(L, f).restype = I
         _lib = L
     return _lib
@@ -315,6 +316,26 @@ def ddt_kv_commit(acc: Accept, c_kv, k_rope, prefix_len, status, stream=None):
     a = acc.c()
     _check(lib().ddt_kv_commit(ctypes.byref(a), B, D, Tcap, _ptr(c_kv), _ptr(k_rope), _ptr(prefix_len),
                                _ptr(status), _stream_ptr(stream)), "ddt_kv_commit")
+
+
+def ddt_tree_sample(tree: Tree, logits, temperature: float, u01=None, sample_tok=None, node_p=None,
+                    stream=None):
+    """Temperature sampling at every tree node. ``logits`` float32
+    [B,Qc,V] (V a multiple of 4), ``u01`` float32 [B,Qc] (not read when
+    temperature <= 0, the greedy limit). Returns (sample_tok int32 [B,Qc],
+    node_p float32 [B,Qc]); pass sample_tok to ddt_tree_accept as its target."""
+    _contig(logits)
+    if u01 is not None:
+        _contig(u01)
+    B, Qc, V = logits.shape
+    if sample_tok is None:
+        sample_tok = torch.empty(B, Qc, dtype=torch.int32, device=logits.device)
+    if node_p is None:
+        node_p = torch.empty(B, Qc, dtype=torch.float32, device=logits.device)
+    t = tree.c()
+    _check(lib().ddt_tree_sample(ctypes.byref(t), _ptr(logits), V, float(temperature), _ptr(u01),
+                                 _ptr(sample_tok), _ptr(node_p), _stream_ptr(stream)), "ddt_tree_sample")
+    return sample_tok, node_p
 
 
 class VerifyStep:

@@ -23,7 +23,16 @@ Recipe (one ``numpy.random.default_rng(20260 + config_index)`` per config):
   even); the prefix length T_b is fixed per config or uniform in an inclusive
   range; node m of sequence b owns KV row T_b + m;
 * target argmax per tree node: with probability p the rank-0 token of the next
-  depth row, else a uniform id (nodes at the last depth always draw uniform).
+  depth row, else a uniform id (nodes at the last depth always draw uniform);
+* target logits per tree node (sampling path): float32 background
+  N(0, sigma^2) over the whole vocabulary; a node at depth d < D then gets the
+  drafter's row-d tokens raised to log(V) + sigma^2 / 2 + lead - step * rank
+  (log(V) + sigma^2 / 2 is about the log of the background's total mass, so
+  the drafter's rank-0 token carries roughly half the probability at
+  temperature 1 and the target agrees with the draft tree often, as a
+  well-matched drafter would); the uniforms for sampling are float32 draws in
+  [0, 1). The sampling draws of config k come from their own
+  ``default_rng(20360 + k)``, after the tree is known.
 """
 from __future__ import annotations
 
@@ -198,3 +207,44 @@ def synth_target_argmax(depth: np.ndarray, n_nodes: np.ndarray, draft_tok: np.nd
             if d < D and u[b, i] < p:
                 out[b, i] = draft_tok[b, d, 0]
     return out
+
+
+def target_logits(rng: np.random.Generator, depth: np.ndarray, n_nodes: np.ndarray,
+                  draft_tok: np.ndarray, vocab: int, sigma: float = 1.5, lead: float = 1.0,
+                  step: float = 1.5) -> np.ndarray:
+    """Synthetic target logits after each tree node: float32 [B,Qc,vocab].
+
+    ``depth`` [B,Qc] and ``n_nodes`` [B] describe a built tree (the caller
+    passes the tree it trusts). Padding slots keep the plain background."""
+    B, Qc = depth.shape
+    D, K = draft_tok.shape[1], draft_tok.shape[2]
+    out = np.empty((B, Qc, vocab), np.float32)
+    for b in range(B):
+        for i in range(Qc):
+            out[b, i] = rng.standard_normal(vocab, dtype=np.float32) * np.float32(sigma)
+    base = math.log(vocab) + sigma * sigma / 2.0
+    boost = (base + lead - step * np.arange(K)).astype(np.float32)
+    for b in range(B):
+        for i in range(int(n_nodes[b])):
+            d = int(depth[b, i])
+            if 0 <= d < D:
+                ids = draft_tok[b, d]
+                keep = ids < vocab  # a smaller vocabulary drops the drafter's larger ids
+                out[b, i, ids[keep]] = boost[keep]
+    return out
+
+
+def sample_uniforms(rng: np.random.Generator, B: int, Qc: int) -> np.ndarray:
+    """float32 uniforms in [0, 1), one per tree node slot: [B,Qc]."""
+    return rng.random((B, Qc), dtype=np.float32)
+
+
+def sampling_inputs(index: int, depth: np.ndarray, n_nodes: np.ndarray, draft_tok: np.ndarray,
+                    vocab: int | None = None):
+    """(logits float32 [B,Qc,V], u01 float32 [B,Qc]) for workload ``index``
+    and the tree given by ``depth`` / ``n_nodes``."""
+    wl = WORKLOADS[index]
+    rng = np.random.default_rng(SEED_BASE + 100 + index)
+    V = wl.vocab if vocab is None else vocab
+    lg = target_logits(rng, depth, n_nodes, draft_tok, V)
+    return lg, sample_uniforms(rng, depth.shape[0], depth.shape[1])

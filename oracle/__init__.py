@@ -53,6 +53,8 @@ def _load():
             lib.ddto_tree_accept.restype = i
             lib.ddto_kv_commit.argtypes = [i, i, i, P, P, P, P, P, P]
             lib.ddto_kv_commit.restype = i
+            lib.ddto_tree_sample.argtypes = [i, i, i, P, ctypes.c_double, P, P, P, P, P, P, P]
+            lib.ddto_tree_sample.restype = i
             _lib = lib
     return _lib
 
@@ -173,3 +175,27 @@ def gather_paged(pool_kv, pool_kr, kv_index):
     kv[~ok] = 0
     kr[~ok] = 0
     return kv, kr
+
+
+def tree_sample(tree: Tree, logits, temperature: float, u01, status=None):
+    """Temperature sampling at every node of the tree (float64).
+
+    ``logits`` float32 [B,Qc,V], ``u01`` float32 [B,Qc]; ``tree`` needs
+    token, parent and n_nodes. Returns (sample_tok int32 [B,Qc], node_p
+    float64 [B,Qc], status int32 [B]); ``status`` (default: all OK) is copied
+    and BADINPUT is set where a row has no distribution or a child token is out
+    of range."""
+    lib = _load()
+    lg = np.ascontiguousarray(logits, np.float32)
+    B, Qc, V = lg.shape
+    uu = np.ascontiguousarray(u01, np.float32).reshape(B, Qc)
+    st = np.zeros(B, np.int32) if status is None else np.array(status, dtype=np.int32, copy=True)
+    tok = np.empty((B, Qc), np.int32)
+    npb = np.empty((B, Qc), np.float64)
+    rc = lib.ddto_tree_sample(B, Qc, V, _p(lg), float(temperature), _p(uu),
+                              _p(np.ascontiguousarray(tree.token, np.int32)),
+                              _p(np.ascontiguousarray(tree.parent, np.int32)),
+                              _p(np.ascontiguousarray(tree.n_nodes, np.int32)), _p(tok), _p(npb), _p(st))
+    if rc != 0:
+        raise MemoryError("ddto_tree_sample: out of host memory")
+    return tok, npb, st

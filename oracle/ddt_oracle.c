@@ -4,7 +4,7 @@
  * and the benchmark's CPU-baseline leg do.  It shares no code, header, table or
  * helper with the CUDA library.
  *
- * Three plain, slow functions, each written from its definition:
+ * Plain, slow functions, each written from its definition:
  *
  *  ddto_tree_build  best-first draft-tree expansion with a binary heap, as the
  *                   per-request CPU builder the GPU builder replaces ("The
@@ -24,6 +24,11 @@
  *                   "Architectural Abstraction").
  *  ddto_tree_accept greedy follow-the-verified-tree walk ("The Architecture of
  *                   Closure", the kernel table row for tree_accept.cu).
+ *  ddto_tree_sample temperature sampling at every tree node by inverse
+ *                   transform, plus each node's probability under its
+ *                   parent's distribution ("The Architecture of a
+ *                   Thousand-Parameter Decision", "What to Reuse" item 3 and
+ *                   "What to Build New" item 2: the sampling-probability path).
  *
  * Readings taken where the pages are silent (each is a choice, documented in
  * the design notes): a node is a rank path (r_1..r_d); its score is the float32
@@ -381,5 +386,130 @@ int ddto_kv_commit(int B, int D, int Tcap, const int32_t *accept_len, const int3
     }
     free(tmp_kv);
     free(tmp_kr);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* temperature sampling over the tree                                  */
+/* ------------------------------------------------------------------ */
+
+/* The sampling commit path ("The Architecture of a Thousand-Parameter
+ * Decision", "What to Reuse" item 3: temperature sampling from the verified
+ * token distribution; "What to Build New" item 2: the sampling-probability
+ * path that normalises the target's probabilities over the tree nodes).
+ *
+ * Row (b, i) of `logits` [B,Qc,V] is the target's logit vector after node i.
+ * Its distribution is p_j = exp((x_j - M) / tau) / S with M = max_j x_j and
+ * S = sum_j exp((x_j - M) / tau).  With one uniform u = u01[b,i] the node's
+ * sample is drawn by inverse transform over token ids in increasing order:
+ * the first token j with p_j > 0 whose cumulative probability C_j exceeds u
+ * (u < 0 therefore gives the first token of nonzero probability); when no
+ * token qualifies (u >= 1, NaN, or rounding at the top) the last token with
+ * p_j > 0.  tau <= 0 is the greedy limit: the first index of the largest
+ * logit.
+ *
+ * node_p[b,c] is the probability the parent's row gives node c's own token
+ * (the normalised probability tree verification needs); node_p[b,0] = 1, and
+ * node slots at or past n_nodes[b] get sample -1 and node_p 0.  In the
+ * greedy limit node_p is 1 for the child whose token is the argmax and 0
+ * otherwise.
+ *
+ * A row holding a NaN, or (tau > 0) whose largest logit is not finite, has
+ * no distribution: its sample is -1, its children's node_p are 0 and the
+ * sequence gets BADINPUT.  A child token outside [0, V) gets node_p 0 and
+ * BADINPUT too.  Everything in float64; sums in token order. */
+static void sample_row(int V, const float *x, double tau, double u, int *tok_out, double *S_out,
+                       double *M_out, int *bad) {
+    int has_nan = 0;
+    double M = -INFINITY;
+    int arg = 0;
+    for (int j = 0; j < V; ++j) {
+        if (x[j] != x[j]) { has_nan = 1; continue; }
+        if ((double)x[j] > M) { M = x[j]; arg = j; }
+    }
+    *M_out = M;
+    *S_out = 0.0;
+    if (has_nan || (tau > 0.0 && !isfinite(M))) {
+        *bad = 1;
+        *tok_out = -1;
+        return;
+    }
+    if (tau <= 0.0) {
+        *tok_out = arg;
+        return;
+    }
+    double S = 0.0;
+    for (int j = 0; j < V; ++j) S += exp(((double)x[j] - M) / tau);
+    *S_out = S;
+    const double thr = u * S;
+    double C = 0.0;
+    int last_pos = -1, pick = -1;
+    for (int j = 0; j < V; ++j) {
+        const double w = exp(((double)x[j] - M) / tau);
+        C += w;
+        if (w > 0.0) {
+            last_pos = j;
+            if (C > thr) { pick = j; break; }
+        }
+    }
+    if (pick < 0) {
+        for (int j = V - 1; j >= 0; --j)
+            if (exp(((double)x[j] - M) / tau) > 0.0) { last_pos = j; break; }
+        pick = last_pos;
+    }
+    *tok_out = pick;
+}
+
+int ddto_tree_sample(int B, int Qc, int V, const float *logits, double tau, const float *u01,
+                     const int32_t *token, const int32_t *parent, const int32_t *n_nodes,
+                     int32_t *sample_tok, double *node_p, int32_t *status) {
+    const long long rows = (long long)B * Qc;
+    double *Ss = (double *)malloc(sizeof(double) * (size_t)rows);
+    double *Ms = (double *)malloc(sizeof(double) * (size_t)rows);
+    int *bad = (int *)calloc((size_t)rows, sizeof(int));
+    if (!Ss || !Ms || !bad) {
+        free(Ss);
+        free(Ms);
+        free(bad);
+        return -1;
+    }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (long long r = 0; r < rows; ++r) {
+        const int b = (int)(r / Qc), i = (int)(r % Qc);
+        int n = n_nodes[b];
+        n = n < 1 ? 1 : (n > Qc ? Qc : n);
+        if (i >= n) {
+            sample_tok[r] = -1;
+            continue;
+        }
+        int t;
+        sample_row(V, logits + (size_t)r * V, tau, (double)u01[r], &t, &Ss[r], &Ms[r], &bad[r]);
+        sample_tok[r] = t;
+    }
+    for (int b = 0; b < B; ++b) {
+        int n = n_nodes[b];
+        n = n < 1 ? 1 : (n > Qc ? Qc : n);
+        const size_t tb = (size_t)b * Qc;
+        int flag = 0;
+        for (int i = 0; i < n; ++i) flag |= bad[tb + i];
+        node_p[tb] = 1.0;
+        for (int c = 1; c < Qc; ++c) {
+            if (c >= n) { node_p[tb + c] = 0.0; continue; }
+            const int pi = parent[tb + c], tk = token[tb + c];
+            const size_t row = tb + (size_t)pi;
+            if (tk < 0 || tk >= V) { node_p[tb + c] = 0.0; flag = 1; continue; }
+            if (bad[row]) { node_p[tb + c] = 0.0; continue; }
+            if (tau <= 0.0)
+                node_p[tb + c] = (sample_tok[row] == tk) ? 1.0 : 0.0;
+            else
+                node_p[tb + c] = exp(((double)logits[row * V + tk] - Ms[row]) / tau) / Ss[row];
+        }
+        if (flag) status[b] = ORACLE_BADINPUT;
+    }
+    free(Ss);
+    free(Ms);
+    free(bad);
     return 0;
 }

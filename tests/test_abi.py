@@ -137,3 +137,25 @@ def test_paged_attention_rejects_missing_block_table(L):
                                        None, 0, None, 8, None) == ddtree.DDT_E_INVAL
     assert L.ddt_verify_mla_attn_paged(ctypes.byref(a), ctypes.byref(t), ctypes.c_float(0.1), ctypes.byref(o),
                                        None, 0, FAKE, 0, None) == ddtree.DDT_E_INVAL
+
+
+def test_tree_sample_rejects_bad_arguments(L):
+    t = _tree()
+    P = ctypes.c_void_p
+
+    def call(tree=t, logits=FAKE, vocab=1000, tau=1.0, u=FAKE, tok=FAKE, p=FAKE):
+        return L.ddt_tree_sample(ctypes.byref(tree) if tree is not None else None, P(logits), vocab,
+                                 ctypes.c_float(tau), P(u), P(tok), P(p), None)
+    assert call(tree=None) == ddtree.DDT_E_INVAL
+    assert call(logits=None) == ddtree.DDT_E_INVAL
+    assert call(logits=FAKE + 4) == ddtree.DDT_E_INVAL       # not 16-byte aligned
+    assert call(vocab=1002) == ddtree.DDT_E_INVAL            # not a multiple of 4
+    assert call(vocab=0) == ddtree.DDT_E_INVAL
+    assert call(tau=float("nan")) == ddtree.DDT_E_INVAL
+    assert call(tau=float("inf")) == ddtree.DDT_E_INVAL
+    assert call(tau=1e-35) == ddtree.DDT_E_INVAL
+    assert call(u=None) == ddtree.DDT_E_INVAL                # sampling needs the uniforms
+    assert call(tok=None) == ddtree.DDT_E_INVAL
+    assert call(p=None) == ddtree.DDT_E_INVAL
+    bad = _tree(Qc=66, W=2)
+    assert call(tree=bad) == ddtree.DDT_E_INVAL
