@@ -60,12 +60,15 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 cudaError_t launch_kv_commit(int B, int D, int Tcap, const int32_t *accept_len, const int32_t *accept_idx,
                              void *c_kv, void *k_rope, int32_t *prefix_len, int32_t *status, cudaStream_t s);
 
-// Temperature sampling at every tree node: C CTAs (one cluster) per row of
-// logits, each holding 1024 * r tokens (r <= kSampleMaxRows).
-constexpr int kSampleMaxRows = 24;
+// Temperature sampling at every tree node: a persistent grid of clusters of
+// C CTAs per row; each CTA owns nreg regions of 128 R tokens (R odd).
+constexpr int kSampleMaxRows = 11;      // R: float4 per lane in a region
+constexpr int kSampleMaxRegions = 128;  // regions per CTA
+constexpr int kSampleListCap = 256;     // rows per cluster and launch
 struct SamplePlan {
     int C;        // CTAs per row (cluster size); 0 = shape not supported
-    int r;        // 128-token rows per warp region
+    int R;        // float4 per lane in a region (odd)
+    int nreg;     // regions per CTA (a multiple of 8)
     size_t smem;  // dynamic shared memory per CTA
 };
 SamplePlan plan_sample(int V, long long rows, int sms, int max_cluster);

@@ -18,29 +18,42 @@
 // samples in place of the greedy argmax (the accept walk) commits tokens
 // distributed exactly as the target's temperature sampling would.
 //
-// Layout of the work. One cluster of C CTAs per row; CTA c holds tokens
-// [c * 1024 r, (c + 1) * 1024 r), split into 8 warp regions of r rows of 128
-// tokens (a row is one float4 per lane). Each warp fetches its region with
-// one bulk copy into shared memory, so the logits are read from HBM once:
-//   pass 1  largest logit (and its first index), NaN check, per warp -> CTA;
-//   pass 2  weights relative to the CTA's own maximum; per row a sum over the
-//           32 lanes in lane order, per warp a prefix over its rows (float32),
-//           per CTA a float64 sum over its warps;
-//   exchange  each CTA publishes (max, first index, sum) in its shared memory;
-//           after a cluster barrier every CTA reads all C summaries through
-//           distributed shared memory and computes the same row maximum, the
-//           same total and the same winning CTA;
-//   locate  the winning CTA descends warp -> row -> lane -> element using the
-//           very sums it built in pass 2 (recomputed weights are bit-identical:
-//           one fixed sequence of correctly rounded operations), so every level
-//           agrees with the level above it up to the rounding of that level's
-//           prefix (float32 inside a CTA, float64 across CTAs); a threshold
-//           that falls past a level's total takes that level's last nonzero
-//           entry.
+// Layout of the work. A persistent grid of clusters of C CTAs; cluster g
+// takes rows g, g + G, g + 2G, ... (G clusters). In a row, CTA c owns tokens
+// [c * NREG * R * 128, (c + 1) * NREG * R * 128), cut into NREG regions of
+// 128 R tokens; warp w takes regions w, w + 8, ... and streams them, row
+// after row, through a two-stage ring of bulk copies into shared memory; the
+// logits are read from HBM once. In a region lane l owns the R consecutive
+// float4 l R .. l R + R - 1 (R odd: the 8 lanes of a 128-bit shared-memory
+// phase then hit 8 different bank groups). C is the smallest cluster that
+// still fills the GPU (two CTAs per SM): every row ends with block-wide (and,
+// for C > 1, cluster-wide) synchronisation, so the longer a CTA's share of a
+// row, the smaller that fixed cost against its streaming time.
+//
+// Per region (one warp):
+//   pass 1  largest logit (NaN-propagating max; the greedy kernel tracks the
+//           first index of the largest instead);
+//   pass 2  weights against the region's largest logit, 4 at a time (a quad
+//           sum), a sequential sum per lane, an inclusive scan over the
+//           lanes (its last entry is the region total).
+// Per row:
+//   CTA      the regions' maxima combine into the CTA's, each region's total
+//           is scaled to it (an exact power of two times a hardware exp2 of
+//           the fraction) and scanned over the regions as a float pair;
+//   cluster  every CTA publishes (max, first index, total) in its shared
+//           memory; after a cluster barrier every CTA reads the C summaries
+//           through distributed shared memory and computes the same row
+//           maximum, float-pair scan, total and winning CTA;
+//   locate   the winning CTA descends region -> lane -> float4 -> element over
+//           the sums it built; for the float4 level it reloads the chosen
+//           lane's R float4 from memory and recomputes their quad sums, which
+//           come out bit-identical (one fixed sequence of correctly rounded
+//           operations). A threshold past a level's total takes that level's
+//           last entry of nonzero weight.
 // Rank 0 of the cluster writes the greedy result and the children's node
 // probabilities (the child token's weight against the row maximum over the
-// row total). Float64 arithmetic runs only in single threads: its rate on
-// this GPU is a small fraction of float32's.
+// row total). No float64: this GPU's float64 rate is a small fraction of
+// float32's, so the sums above a lane are float pairs (hi + lo).
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -56,32 +69,31 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kRowTokens = 128;           // one float4 per lane
-constexpr int kFlagNan = 1, kFlagTimeout = 2;
+constexpr int kStages = 2;  // ring depth per warp
+constexpr int kFlagNan = 1, kFlagTimeout = 2, kFlagNoDist = 4;
 
 struct Ctrl {
-    uint64_t bar[kWarps];         // one bulk copy per warp region
-    float incl[kWarps][32];       // inclusive prefix over each region's row sums
-    float rsum[kWarps][32];       // row sums (lane order)
-    float wsum[kWarps];           // region totals
-    float wmax[kWarps];
-    int widx[kWarps];
-    int wflag[kWarps];
-    // published to the cluster
-    double pub_s;
-    float pub_m;
-    int pub_idx;
-    int pub_flag;
+    uint64_t bar[kWarps][kStages];
+    float rmax[kSampleMaxRegions];   // region maximum
+    int ridx[kSampleMaxRegions];     // its first index (greedy)
+    int rflag[kSampleMaxRegions];
+    float rtot[kSampleMaxRegions];   // region total, units of 2^((x - rmax) kd)
+    unsigned lpos[kSampleMaxRegions];  // lanes of the region with nonzero weight
+    float fscale[kSampleMaxRegions]; // 2^((rmax - m_c) kd)
+    float mass_hi[kSampleMaxRegions], mass_lo[kSampleMaxRegions];  // rtot * fscale
+    float scan_hi[kSampleMaxRegions], scan_lo[kSampleMaxRegions];  // inclusive scan of mass
+    float quads[32];                 // the located lane's quad sums
+    // published to the cluster, double-buffered by row parity
+    float pub_m[2], pub_hi[2], pub_lo[2];
+    int pub_idx[2], pub_flag[2];
     // the row's result, identical in every CTA of the cluster
-    int row_flag;                 // kFlag* bits; 4: no distribution
-    int row_idx;                  // first index of the largest logit
-    int cstar;                    // CTA holding the sample
-    float row_m;
-    float row_s;                  // the row's total weight (in units of 2^((x - row_m) kd))
-    float t_cta;                  // threshold inside CTA cstar, in its own weight units
-    double s_c;                   // this CTA's total (float64 sum of the region totals)
-    double xps[16];               // the cluster's CTA totals and scales, for one thread
-    float xfc[16];
+    int row_flag, row_idx, cstar;
+    float row_m, row_s, t_hi, t_lo;
+    // the cluster's rows that hold a node (padding slots left out), in order
+    int nlist;
+    int wcount[kWarps];
+    int list_row[kSampleListCap];
+    int list_n[kSampleListCap];
 };
 
 struct SampleArgs {
@@ -93,8 +105,9 @@ struct SampleArgs {
     int32_t *sample_tok;
     float *node_p;
     int32_t *status;
-    double kd;  // log2(e) / temperature; 0 selects the greedy limit
-    int Qc, V, C, r;
+    float kh, kl;        // log2(e) / temperature = kh + kl, kl > 0 (unused by the greedy kernel)
+    int row0, rows_end;  // this launch's rows: cluster g takes row0 + g + t * G < rows_end
+    int Qc, V, C, R, nreg, G;
 };
 
 // Bulk copy global -> this CTA's shared memory, credited to `bar`.
@@ -115,38 +128,104 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
     asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
     return v;
 }
-__device__ __forceinline__ double ld_cluster_f64(uint32_t a) {
-    double v;
-    asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(a) : "memory");
-    return v;
+
+// max that returns NaN when either operand is NaN
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
 }
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint64_t deadline) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
+    const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
     for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, 0)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 63u && globaltimer_ns() > deadline) return false;
     }
 }
 
-// Weight of logit x against the reference m: 2^((x - m) kd), kd carried as a
-// float pair (kh + kl) so the product keeps about 48 bits of it. Every
-// operation is explicitly rounded (no contraction), so the same inputs give
-// the same bits wherever this is evaluated.
+// Weight of logit x against the reference m: 2^((x - m) kd), kd carried as
+// kh + kl with kl > 0 (so x = -inf gives -inf * kl = -inf, weight 0, and a
+// NaN propagates). Every operation is explicitly rounded (no contraction), so
+// the same inputs give the same bits wherever this is evaluated.
 __device__ __forceinline__ float weight(float x, float m, float kh, float kl) {
     const float d = __fsub_rn(x, m);
-    const float arg = __fmaf_rn(d, kh, __fmul_rn(d, kl));
-    return x == -INFINITY ? 0.f : ex2_approx(arg);
+    return ex2_approx(__fmaf_rn(d, kh, __fmul_rn(d, kl)));
 }
 
-__device__ __forceinline__ void quad_weights(const float4 v, float m, float kh, float kl, float (&e)[4]) {
-    e[0] = weight(v.x, m, kh, kl);
-    e[1] = weight(v.y, m, kh, kl);
-    e[2] = weight(v.z, m, kh, kl);
-    e[3] = weight(v.w, m, kh, kl);
+__device__ __forceinline__ float quad_sum(const float4 v, float m, float kh, float kl) {
+    const float e0 = weight(v.x, m, kh, kl), e1 = weight(v.y, m, kh, kl);
+    const float e2 = weight(v.z, m, kh, kl), e3 = weight(v.w, m, kh, kl);
+    return __fadd_rn(__fadd_rn(__fadd_rn(e0, e1), e2), e3);
 }
 
-__device__ __forceinline__ float quad_sum(const float (&e)[4]) {
-    return __fadd_rn(__fadd_rn(__fadd_rn(e[0], e[1]), e[2]), e[3]);
+// 2^((a - b) kd) for a <= b with an exponent good to far below float32
+// rounding: a - b as an exact float pair (two-sum), its product with
+// kd = kh + kl as a float pair (the fma residual), the integer part of the
+// exponent applied exactly (ldexpf) and only the fraction through exp2.
+__device__ __forceinline__ float exp2_diff(float a, float b, float kh, float kl) {
+    if (a == -INFINITY) return 0.f;
+    const float nb = -b;
+    const float s = __fadd_rn(a, nb);
+    const float bv = __fsub_rn(s, a);
+    const float av = __fsub_rn(s, bv);
+    const float err = __fadd_rn(__fsub_rn(a, av), __fsub_rn(nb, bv));  // s + err == a - b exactly
+    const float ph = __fmul_rn(s, kh);
+    if (ph < -250.f) return 0.f;
+    const float pl = __fmaf_rn(s, kh, -ph);
+    const float rest = __fadd_rn(pl, __fadd_rn(__fmul_rn(s, kl), __fmul_rn(err, kh)));
+    const float n = rintf(ph);
+    const float frac = __fadd_rn(__fsub_rn(ph, n), rest);
+    return ldexpf(ex2_approx(frac), static_cast<int>(n));
+}
+
+// ---- float pairs (hi + lo, |lo| <= ulp(hi) / 2): sums of up to a few
+// thousand terms with about 44 significant bits, all in float32
+struct ff {
+    float hi, lo;
+};
+__device__ __forceinline__ ff ff_norm(float s, float e) {  // |s| >= |e|
+    const float hi = __fadd_rn(s, e);
+    return {hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+    const float s = __fadd_rn(a.hi, b.hi);
+    const float bv = __fsub_rn(s, a.hi);
+    const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bv)), __fsub_rn(b.hi, bv));
+    return ff_norm(s, __fadd_rn(err, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ ff ff_neg(ff a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ ff ff_mul(ff a, float f) {
+    const float p = __fmul_rn(a.hi, f);
+    return ff_norm(p, __fmaf_rn(a.lo, f, __fmaf_rn(a.hi, f, -p)));
+}
+__device__ __forceinline__ ff ff_div(ff a, float f) {
+    const float q1 = __fdiv_rn(a.hi, f);
+    const float r = __fadd_rn(__fmaf_rn(-q1, f, a.hi), a.lo);
+    return ff_norm(q1, __fdiv_rn(r, f));
+}
+__device__ __forceinline__ bool ff_gt(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+__device__ __forceinline__ ff ff_shfl(ff a, int src) {
+    return {__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
+}
+// inclusive scan over the lanes, fixed association
+__device__ __forceinline__ ff ff_scan(ff v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const ff u = {__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+        if (lane >= o) v = ff_add(u, v);
+    }
+    return v;
+}
+
+// inclusive scan over the lanes in float32, fixed association
+__device__ __forceinline__ float warp_scan(float v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v = __fadd_rn(u, v);
+    }
+    return v;
 }
 
 __device__ __forceinline__ void consider(float x, int j, float &best, int &bidx, int &flag) {
@@ -157,336 +236,436 @@ __device__ __forceinline__ void consider(float x, int j, float &best, int &bidx,
     }
 }
 
-// First set bit of `pick`, else the highest set bit of `pos` (-1 if none).
-__device__ __forceinline__ int choose(unsigned pick, unsigned pos) {
-    if (pick) return __ffs(pick) - 1;
-    return pos ? 31 - __clz(pos) : -1;
-}
-
-__global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int r = a.r, C = a.C, V = a.V, Qc = a.Qc;
-    const int row = blockIdx.x / C;
-    const int rank = static_cast<int>(cluster_ctarank());
-    const int b = row / Qc, i = row - b * Qc;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const unsigned full = 0xffffffffu;
-    int n = a.n_nodes[b];
-    n = n < 1 ? 1 : (n > Qc ? Qc : n);
-    if (i >= n) {  // a padding slot: the whole cluster leaves before any exchange
-        if (rank == 0 && threadIdx.x == 0) {
-            a.sample_tok[row] = -1;
-            a.node_p[row] = 0.f;
-        }
-        return;
-    }
-    const bool greedy = a.kd == 0.0;
-    float *data = reinterpret_cast<float *>(smem);
-    float *tiles = data + kWarps * r * kRowTokens;
-    Ctrl &ct = *reinterpret_cast<Ctrl *>(smem + static_cast<size_t>(r) * 5120);
-
-    // ---- fetch this warp's region
-    const long long cta0 = static_cast<long long>(rank) * r * (kWarps * kRowTokens);
-    const long long reg0 = cta0 + static_cast<long long>(warp) * r * kRowTokens;
-    const long long left = static_cast<long long>(V) - reg0;
-    const int nvalid = left <= 0 ? 0 : (left >= r * kRowTokens ? r * kRowTokens : static_cast<int>(left));
-    const int nq = nvalid >> 2;
-    float *reg = data + warp * r * kRowTokens;
-    const float4 *reg4 = reinterpret_cast<const float4 *>(reg);
-    const uint32_t bar = smem_u32(&ct.bar[warp]);
-    if (lane == 0) {
-        mbar_init(bar, 1);
-        mbar_fence_init();
-        if (nvalid > 0) {
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nvalid) * 4u);
-            bulk_load(smem_u32(reg), a.logits + static_cast<size_t>(row) * V + reg0,
-                      static_cast<uint32_t>(nvalid) * 4u, bar);
-        }
-    }
-    __syncwarp();
-    int flag = 0;
-    if (nvalid > 0 && !wait_bar(bar, globaltimer_ns() + kWaitLimitNs)) flag |= kFlagTimeout;
-
-    // ---- pass 1: largest logit, its first index, NaN check
-    float best = -INFINITY;
-    int bidx = INT_MAX;
-    if (!(flag & kFlagTimeout)) {
-        for (int k = 0; k < r; ++k) {
-            const int q = k * 32 + lane;
-            if (q < nq) {
-                const float4 v = reg4[q];
-                const int j = static_cast<int>(reg0) + 4 * q;
-                consider(v.x, j, best, bidx, flag);
-                consider(v.y, j + 1, best, bidx, flag);
-                consider(v.z, j + 2, best, bidx, flag);
-                consider(v.w, j + 3, best, bidx, flag);
-            }
-        }
-    }
+// Larger value, or the lower index among equal values; flags OR-ed; the
+// same result lands in every lane.
+__device__ __forceinline__ void warp_argmax(float &v, int &idx, int &flag) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
-        const float ob = __shfl_xor_sync(full, best, o);
-        const int oi = __shfl_xor_sync(full, bidx, o);
-        flag |= __shfl_xor_sync(full, flag, o);
-        if (ob > best || (ob == best && oi < bidx)) {
-            best = ob;
-            bidx = oi;
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+        flag |= __shfl_xor_sync(0xffffffffu, flag, o);
+        if (ov > v || (ov == v && oi < idx)) {
+            v = ov;
+            idx = oi;
         }
     }
+}
+
+// First lane of `pick`, else the highest lane of `pos` (0 if neither: the
+// callers only reach a level whose total is positive).
+__device__ __forceinline__ int choose(unsigned pick, unsigned pos) {
+    if (pick) return __ffs(pick) - 1;
+    return pos ? 31 - __clz(pos) : 0;
+}
+
+// Node count of sequence b, clamped to [1, Qc].
+__device__ __forceinline__ int node_count(const SampleArgs &a, int b) {
+    const int n = a.n_nodes[b];
+    return n < 1 ? 1 : (n > a.Qc ? a.Qc : n);
+}
+
+template <bool kGreedy>
+__global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int C = a.C, V = a.V, Qc = a.Qc, R = a.R, NREG = a.nreg, G = a.G;
+    const int Q = NREG / kWarps;  // regions per warp per row
+    const int g = blockIdx.x / C;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned full = 0xffffffffu;
+    const float kh = a.kh, kl = a.kl;
+    const int rtok = R * 128;  // tokens per region
+    const long long cta0 = static_cast<long long>(rank) * NREG * rtok;
+    float *stages = reinterpret_cast<float *>(smem);  // [warp][stage][rtok]
+    float *lscan = stages + kWarps * kStages * rtok;  // [region][32] inclusive scan of the lane sums
+    Ctrl &ct = *reinterpret_cast<Ctrl *>(lscan + NREG * 32);
+
     if (lane == 0) {
-        ct.wmax[warp] = best;
-        ct.widx[warp] = bidx;
-        ct.wflag[warp] = flag;
+        for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&ct.bar[warp][s]), 1);
+        mbar_fence_init();
     }
-    __syncthreads();
-    float m_c = -INFINITY;
-    int idx_c = INT_MAX, flag_c = 0;
-    for (int w = 0; w < kWarps; ++w) {
-        const float v = ct.wmax[w];
-        const int ix = ct.widx[w];
-        flag_c |= ct.wflag[w];
-        if (v > m_c || (v == m_c && ix < idx_c)) {
-            m_c = v;
-            idx_c = ix;
+    // ---- the cluster's rows that hold a node, compacted in order (every CTA
+    // of the cluster builds the same list); padding slots get their outputs here
+    {
+        const int span = (a.rows_end - a.row0 - g + G - 1) / G;
+        int base = 0;
+        for (int t0 = 0; t0 < span; t0 += kThreads) {
+            const int t = t0 + threadIdx.x;
+            const int row = a.row0 + g + t * G;
+            bool valid = false;
+            int n = 0;
+            if (t < span) {
+                const int b = row / Qc;
+                n = node_count(a, b);
+                valid = row - b * Qc < n;
+                if (!valid && rank == 0) {
+                    a.sample_tok[row] = -1;
+                    a.node_p[row] = 0.f;
+                }
+            }
+            const unsigned bal = __ballot_sync(full, valid);
+            if (lane == 0) ct.wcount[warp] = __popc(bal);
+            __syncthreads();
+            int off = base;
+            for (int w = 0; w < warp; ++w) off += ct.wcount[w];
+            if (valid) {
+                const int pos = off + __popc(bal & ((1u << lane) - 1u));
+                ct.list_row[pos] = row;
+                ct.list_n[pos] = n;
+            }
+            for (int w = 0; w < kWarps; ++w) base += ct.wcount[w];
+            __syncthreads();
         }
+        if (threadIdx.x == 0) ct.nlist = base;
+        __syncthreads();
     }
+    const int nlist = ct.nlist;
 
-    // ---- pass 2: weights against m_c; row sums in lane order; float64 prefix over rows
-    const bool weigh = !greedy && flag_c == 0 && m_c > -INFINITY && m_c < INFINITY;
-    float *tile = tiles + warp * r * 32;
-    const float kh = static_cast<float>(a.kd);
-    const float kl = static_cast<float>(a.kd - static_cast<double>(kh));
-    if (weigh) {
-        for (int k = 0; k < r; ++k) {
-            const int q = k * 32 + lane;
-            float s = 0.f;
-            if (q < nq) {
-                float e[4];
-                quad_weights(reg4[q], m_c, kh, kl, e);
-                s = quad_sum(e);
-            }
-            // row k, lane l at column (l + k) mod 32: the row sums below read
-            // a different bank in every lane
-            tile[k * 32 + ((lane + k) & 31)] = s;
+    // ---- producer (lane 0 of each warp): this warp's regions of the
+    // cluster's rows, in order, two in flight
+    int pl = 0, pq = 0;
+    uint32_t issued = 0;
+    auto issue = [&]() {
+        if (pl >= nlist) return;
+        const int prow = ct.list_row[pl];
+        const int stage = static_cast<int>(issued & 1u);
+        const uint32_t bar = smem_u32(&ct.bar[warp][stage]);
+        const long long reg0 = cta0 + static_cast<long long>(warp + kWarps * pq) * rtok;
+        const long long left = static_cast<long long>(V) - reg0;
+        const int nvalid = left <= 0 ? 0 : (left >= rtok ? rtok : static_cast<int>(left));
+        if (nvalid > 0) {
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nvalid) * 4u);
+            bulk_load(smem_u32(stages + (warp * kStages + stage) * rtok),
+                      a.logits + static_cast<size_t>(prow) * V + reg0, static_cast<uint32_t>(nvalid) * 4u, bar);
+        } else {
+            mbar_arrive(bar);  // an empty region still completes its phase
         }
-        __syncwarp();
-        float s = 0.f;
-        if (lane < r) {
-            const float *t = tile + lane * 32;
-            for (int l = 0; l < 32; ++l) s = __fadd_rn(s, t[(l + lane) & 31]);
+        ++issued;
+        if (++pq == Q) {
+            pq = 0;
+            ++pl;
         }
-        ct.rsum[warp][lane] = s;
-        __syncwarp();
-        if (lane == 0) {
-            float acc = 0.f;
-            for (int k = 0; k < r; ++k) {
-                acc = __fadd_rn(acc, ct.rsum[warp][k]);
-                ct.incl[warp][k] = acc;
-            }
-            ct.wsum[warp] = acc;
-        }
-    } else if (lane == 0) {
-        ct.wsum[warp] = 0.f;
+    };
+    if (lane == 0) {
+        issue();
+        issue();
     }
-    __syncthreads();
+    __syncwarp();
 
-    // ---- exchange through distributed shared memory (float64 only in
-    // single threads: this GPU's float64 rate is low)
-    if (threadIdx.x == 0) {
-        double s_c = 0.0;
-        for (int w = 0; w < kWarps; ++w) s_c = __dadd_rn(s_c, static_cast<double>(ct.wsum[w]));
-        ct.s_c = s_c;
-        ct.pub_s = s_c;
-        ct.pub_m = m_c;
-        ct.pub_idx = idx_c;
-        ct.pub_flag = flag_c;
-    }
-    cluster_sync();
-    if (warp == 0) {
-        float pm = -INFINITY;
-        int pi = INT_MAX, pf = 0;
-        double ps = 0.0;
-        if (lane < C) {
-            pm = ld_cluster_f32(mapa_shared(smem_u32(&ct.pub_m), lane));
-            pi = ld_cluster_s32(mapa_shared(smem_u32(&ct.pub_idx), lane));
-            pf = ld_cluster_s32(mapa_shared(smem_u32(&ct.pub_flag), lane));
-            ps = ld_cluster_f64(mapa_shared(smem_u32(&ct.pub_s), lane));
+    uint32_t used = 0;  // regions consumed by this warp
+    int parity = 0;     // row count parity (publication buffer)
+    for (int li = 0; li < nlist; ++li) {
+        const int row = ct.list_row[li], n = ct.list_n[li];
+        const int b = row / Qc, i = row - b * Qc;
+        const size_t tb = static_cast<size_t>(b) * Qc;
+        // loads the end of the row needs, issued now so they land during the
+        // region passes: the uniform (warp 0), the children of node i (rank 0)
+        const float u = (!kGreedy && warp == 0) ? a.u01[row] : 0.f;
+        const int c = threadIdx.x;
+        int c_par = -1, c_tok = -1;
+        if (rank == 0 && c >= 1 && c < n) {
+            c_par = a.parent[tb + c];
+            c_tok = a.token[tb + c];
         }
-        float M = pm;
-        int idx = pi, f = pf;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const float ob = __shfl_xor_sync(full, M, o);
-            const int oi = __shfl_xor_sync(full, idx, o);
-            f |= __shfl_xor_sync(full, f, o);
-            if (ob > M || (ob == M && oi < idx)) {
-                M = ob;
-                idx = oi;
-            }
-        }
-        if (!greedy && !(M > -INFINITY && M < INFINITY)) f |= 4;
-        // CTA c's scale 2^((m_c - M) kd): the exponent in float64 (exact
-        // difference), its fraction through the hardware exp2, the integer
-        // part applied exactly
-        float fc = 0.f;
-        if (!greedy && f == 0 && lane < C && pm > -INFINITY) {
-            const double e = (static_cast<double>(pm) - static_cast<double>(M)) * a.kd;
-            const double fl = floor(e);
-            fc = fl < -126.0 ? 0.f : ldexpf(ex2_approx(static_cast<float>(e - fl)), static_cast<int>(fl));
-        }
-        if (lane < C) {
-            ct.xfc[lane] = fc;
-            ct.xps[lane] = ps;
-        }
-        __syncwarp();
-        if (lane == 0) {
-            int cstar = 0;
-            float S_f = 0.f, t = 0.f;
-            if (!greedy && f == 0) {
-                // the CTA holding M has a weight-1 element: S >= 1, and some
-                // CTA has positive mass
-                double S = 0.0;
-                for (int c = 0; c < C; ++c) S = __dadd_rn(S, static_cast<double>(ct.xfc[c]) * ct.xps[c]);
-                const double thr = static_cast<double>(a.u01[row]) * S;
-                double pre = 0.0, pre_star = 0.0;
-                int last = -1, pick = -1;
-                for (int c = 0; c < C; ++c) {
-                    const double mc = static_cast<double>(ct.xfc[c]) * ct.xps[c];
-                    if (mc > 0.0) {
-                        last = c;
-                        pre_star = pre;
-                        if (__dadd_rn(pre, mc) > thr) {
-                            pick = c;
-                            break;
+
+        // ---- this warp's regions of the row
+        for (int q = 0; q < Q; ++q) {
+            const int j = warp + kWarps * q;
+            const int stage = static_cast<int>(used & 1u);
+            const long long reg0 = cta0 + static_cast<long long>(j) * rtok;
+            const long long left = static_cast<long long>(V) - reg0;
+            const int nq = (left <= 0 ? 0 : (left >= rtok ? rtok : static_cast<int>(left))) >> 2;
+            int flag = 0;
+            if (!wait_bar(smem_u32(&ct.bar[warp][stage]), (used >> 1) & 1u)) flag |= kFlagTimeout;
+            const int q0 = lane * R;  // this lane's first float4 of the region
+            const float4 *reg4 = reinterpret_cast<const float4 *>(stages + (warp * kStages + stage) * rtok) + q0;
+            float best = -INFINITY;
+            int bidx = INT_MAX;
+            float tot = 0.f;
+            if (kGreedy) {
+                if (!(flag & kFlagTimeout)) {
+                    for (int k = 0; k < R; ++k) {
+                        if (q0 + k < nq) {
+                            const float4 v = reg4[k];
+                            const int t = static_cast<int>(reg0) + 4 * (q0 + k);
+                            consider(v.x, t, best, bidx, flag);
+                            consider(v.y, t + 1, best, bidx, flag);
+                            consider(v.z, t + 2, best, bidx, flag);
+                            consider(v.w, t + 3, best, bidx, flag);
                         }
                     }
-                    pre = __dadd_rn(pre, mc);
                 }
-                cstar = pick >= 0 ? pick : last;
-                t = static_cast<float>((thr - pre_star) / static_cast<double>(ct.xfc[cstar]));
-                S_f = static_cast<float>(S);
+                warp_argmax(best, bidx, flag);
+            } else {
+                // pass 1: NaN-propagating max
+                if (!(flag & kFlagTimeout)) {
+                    for (int k = 0; k < R; ++k) {
+                        if (q0 + k < nq) {
+                            const float4 v = reg4[k];
+                            best = max_nan(max_nan(best, v.x), max_nan(v.y, max_nan(v.z, v.w)));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o; o >>= 1) {
+                    best = max_nan(best, __shfl_xor_sync(full, best, o));
+                    flag |= __shfl_xor_sync(full, flag, o);
+                }
+                if (best != best) flag |= kFlagNan;
+                // pass 2: quad sums, a sequential sum per lane, a scan over lanes
+                if (flag == 0 && best > -INFINITY && best < INFINITY) {
+                    float s = 0.f;
+                    for (int k = 0; k < R; ++k)
+                        if (q0 + k < nq) s = __fadd_rn(s, quad_sum(reg4[k], best, kh, kl));
+                    const float inc = warp_scan(s, lane);
+                    lscan[j * 32 + lane] = inc;
+                    const unsigned lp = __ballot_sync(full, s > 0.f);
+                    if (lane == 0) ct.lpos[j] = lp;
+                    tot = __shfl_sync(full, inc, 31);
+                }
             }
-            ct.row_flag = f;
-            ct.row_idx = idx;
-            ct.row_m = M;
-            ct.row_s = S_f;
-            ct.cstar = cstar;
-            ct.t_cta = t;
+            if (lane == 0) {
+                ct.rmax[j] = best;
+                ct.ridx[j] = bidx;
+                ct.rflag[j] = flag;
+                ct.rtot[j] = tot;
+            }
+            __syncwarp();  // every lane is done with the stage
+            ++used;
+            if (lane == 0) issue();
         }
-    }
-    cluster_arrive_release();  // done reading the other CTAs' shared memory
-    __syncthreads();
-    const int rflag = ct.row_flag;
+        // the child's logit (used after the exchange)
+        const bool child = c_par == i;
+        const bool tok_ok = c_tok >= 0 && c_tok < V;
+        const float c_x = (child && tok_ok && !kGreedy) ? a.logits[static_cast<size_t>(row) * V + c_tok] : 0.f;
+        __syncthreads();
 
-    // ---- locate the sample inside the winning CTA
-    if (!greedy && rflag == 0 && rank == ct.cstar && warp == 0) {
-        const float tc = ct.t_cta;
-        // warp region: prefix over the region totals in the order that made s_c
-        int wst = -1, lastw = -1;
-        float pre = 0.f, prel = 0.f;
-        for (int w = 0; w < kWarps; ++w) {
-            const float m = ct.wsum[w];
-            if (m > 0.f) {
-                lastw = w;
-                prel = pre;
-                if (__fadd_rn(pre, m) > tc) {
-                    wst = w;
+        // ---- CTA summary (warp 0)
+        if (warp == 0) {
+            float m = -INFINITY;
+            int idx = INT_MAX, f = 0;
+            for (int j = lane; j < NREG; j += 32) {  // regions in token order
+                const float v = ct.rmax[j];
+                const int ix = ct.ridx[j];
+                f |= ct.rflag[j];
+                if (v > m || (v == m && ix < idx)) {
+                    m = v;
+                    idx = ix;
+                }
+            }
+            warp_argmax(m, idx, f);
+            ff total = {0.f, 0.f};
+            if (!kGreedy && f == 0 && m > -INFINITY && m < INFINITY) {
+                for (int j0 = 0; j0 < NREG; j0 += 32) {
+                    const int j = j0 + lane;
+                    float fs = 0.f;
+                    ff mass = {0.f, 0.f};
+                    if (j < NREG) {
+                        fs = exp2_diff(ct.rmax[j], m, kh, kl);
+                        mass = ff_mul({ct.rtot[j], 0.f}, fs);
+                    }
+                    const ff sc = ff_add(total, ff_scan(mass, lane));
+                    if (j < NREG) {
+                        ct.fscale[j] = fs;
+                        ct.mass_hi[j] = mass.hi;
+                        ct.mass_lo[j] = mass.lo;
+                        ct.scan_hi[j] = sc.hi;
+                        ct.scan_lo[j] = sc.lo;
+                    }
+                    total = ff_shfl(sc, 31);
+                }
+            }
+            if (lane == 0) {
+                ct.pub_m[parity] = m;
+                ct.pub_idx[parity] = idx;
+                ct.pub_flag[parity] = f;
+                ct.pub_hi[parity] = total.hi;
+                ct.pub_lo[parity] = total.lo;
+            }
+        }
+        cluster_sync();
+
+        // ---- cluster exchange (warp 0 of every CTA computes the same result)
+        if (warp == 0) {
+            float pm = -INFINITY;
+            ff ps = {0.f, 0.f};
+            int pi = INT_MAX, pf = 0;
+            if (lane < C) {
+                pm = ld_cluster_f32(mapa_shared(smem_u32(&ct.pub_m[parity]), lane));
+                ps.hi = ld_cluster_f32(mapa_shared(smem_u32(&ct.pub_hi[parity]), lane));
+                ps.lo = ld_cluster_f32(mapa_shared(smem_u32(&ct.pub_lo[parity]), lane));
+                pi = ld_cluster_s32(mapa_shared(smem_u32(&ct.pub_idx[parity]), lane));
+                pf = ld_cluster_s32(mapa_shared(smem_u32(&ct.pub_flag[parity]), lane));
+            }
+            float M = pm;
+            int idx = pi, f = pf;
+            warp_argmax(M, idx, f);
+            if (!kGreedy && !(M > -INFINITY && M < INFINITY)) f |= kFlagNoDist;
+            int cstar = 0;
+            ff S = {0.f, 0.f}, t = {0.f, 0.f};
+            if (!kGreedy && f == 0) {
+                // the CTA holding M has a weight-1 element: S >= 1
+                const float fc = lane < C ? exp2_diff(pm, M, kh, kl) : 0.f;
+                const ff mass = ff_mul(ps, fc);
+                const ff sc = ff_scan(mass, lane);
+                S = ff_shfl(sc, 31);
+                const ff thr = ff_mul(S, u);
+                cstar = choose(__ballot_sync(full, mass.hi > 0.f && ff_gt(sc, thr)), __ballot_sync(full, mass.hi > 0.f));
+                const ff pre = ff_shfl(sc, cstar > 0 ? cstar - 1 : 0);
+                t = ff_div(ff_add(thr, ff_neg(cstar > 0 ? pre : ff{0.f, 0.f})), __shfl_sync(full, fc, cstar));
+            }
+            if (lane == 0) {
+                ct.row_flag = f;
+                ct.row_idx = idx;
+                ct.row_m = M;
+                ct.row_s = S.hi;
+                ct.cstar = cstar;
+                ct.t_hi = t.hi;
+                ct.t_lo = t.lo;
+            }
+        }
+        __syncthreads();
+        const int rflag = ct.row_flag;
+
+        // ---- locate the sample inside the winning CTA (warp 0)
+        if (!kGreedy && rflag == 0 && rank == ct.cstar && warp == 0) {
+            const ff tc = {ct.t_hi, ct.t_lo};
+            // region: first of positive mass whose scan passes tc, else the
+            // last of positive mass
+            int jst = -1, jlast = 0;
+            for (int j0 = 0; j0 < NREG; j0 += 32) {
+                const int j = j0 + lane;
+                const bool pos = j < NREG && ct.mass_hi[j] > 0.f;
+                const unsigned pick = __ballot_sync(full, pos && ff_gt({ct.scan_hi[j], ct.scan_lo[j]}, tc));
+                const unsigned any = __ballot_sync(full, pos);
+                if (pick) {
+                    jst = j0 + __ffs(pick) - 1;
                     break;
                 }
+                if (any) jlast = j0 + 31 - __clz(any);
             }
-            pre = __fadd_rn(pre, m);
-        }
-        if (wst < 0) wst = lastw < 0 ? 0 : lastw;  // (lastw >= 0: this CTA's total is positive)
-        const float tw = __fsub_rn(tc, prel);
-        // row: incl[k] = incl[k-1] + rsum[k], exactly as pass 2 built it
-        const float rs = lane < r ? ct.rsum[wst][lane] : 0.f;
-        const float inc = lane < r ? ct.incl[wst][lane] : 0.f;
-        const int kst =
-            max(0, choose(__ballot_sync(full, rs > 0.f && inc > tw), __ballot_sync(full, rs > 0.f)));
-        const float tk = __fsub_rn(tw, kst > 0 ? ct.incl[wst][kst - 1] : 0.f);
-        // lane: prefix over lanes in lane order, the sequence that made rsum[kst]
-        const float *t = tiles + wst * r * 32 + kst * 32;
-        float p = 0.f, own = 0.f;
-        for (int l = 0; l < 32; ++l) {
-            const float v = t[(l + kst) & 31];
-            if (l <= lane) p = __fadd_rn(p, v);
-            if (l == lane) own = v;
-        }
-        const int lst = max(0, choose(__ballot_sync(full, own > 0.f && p > tk), __ballot_sync(full, own > 0.f)));
-        const float before = __shfl_sync(full, p, lst > 0 ? lst - 1 : 0);
-        const float tl = __fsub_rn(tk, lst > 0 ? before : 0.f);
-        if (lane == 0) {
-            // element: the float4's own partial sums
-            const int q = kst * 32 + lst;
-            const float4 v = reinterpret_cast<const float4 *>(data + wst * r * kRowTokens)[q];
-            float e[4];
-            quad_weights(v, m_c, kh, kl, e);
-            float acc = 0.f;
-            int pick = -1, lastpos = -1;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                acc = j == 0 ? e[0] : __fadd_rn(acc, e[j]);
-                if (e[j] > 0.f) {
-                    lastpos = j;
-                    if (pick < 0 && acc > tl) pick = j;
-                }
-            }
-            const int j = pick >= 0 ? pick : (lastpos >= 0 ? lastpos : 0);
-            a.sample_tok[row] = static_cast<int>(cta0) + wst * r * kRowTokens + 4 * q + j;
-        }
-    }
-
-    // ---- greedy result, flagged rows, node probabilities (rank 0)
-    if (rank == 0) {
-        const size_t tb = static_cast<size_t>(b) * Qc;
-        const int idx = ct.row_idx == INT_MAX ? 0 : ct.row_idx;
-        if (threadIdx.x == 0) {
-            if (rflag != 0) {
-                a.sample_tok[row] = -1;
-                a.status[b] = (rflag & kFlagTimeout) ? DDT_E_TIMEOUT : DDT_E_BADINPUT;
-            } else if (greedy) {
-                a.sample_tok[row] = idx;
-            }
-            if (i == 0) a.node_p[tb] = 1.f;
-        }
-        const int c = threadIdx.x;
-        if (c >= 1 && c < n && a.parent[tb + c] == i) {
-            const int tk = a.token[tb + c];
+            if (jst < 0) jst = jlast;
+            const ff pre_j = jst > 0 ? ff{ct.scan_hi[jst - 1], ct.scan_lo[jst - 1]} : ff{0.f, 0.f};
+            const ff tjf = ff_div(ff_add(tc, ff_neg(pre_j)), ct.fscale[jst]);
+            const float tj = __fadd_rn(tjf.hi, tjf.lo);
+            // lane: the region's lane scan, among the lanes of nonzero weight
+            // (the scan's fixed tree need not rise by an empty lane's zero)
+            const float inc = lscan[jst * 32 + lane];
+            const unsigned lposm = ct.lpos[jst];
+            const bool lpos = (lposm >> lane) & 1u;
+            const int lst = choose(__ballot_sync(full, lpos && inc > tj), lposm);
+            const float tl = __fsub_rn(tj, lst > 0 ? lscan[jst * 32 + lst - 1] : 0.f);
+            // float4 of the lane: its quad sums again, from the logits in
+            // memory, and their sequential prefix (the sequence that made the
+            // lane sum)
+            const float mr = ct.rmax[jst];
+            const long long ltok0 = cta0 + static_cast<long long>(jst) * rtok + 4LL * lst * R;
+            const long long mytok = ltok0 + 4LL * lane;
+            const bool inb = lane < R && mytok + 4 <= V;
+            const float4 v = inb ? *reinterpret_cast<const float4 *>(a.logits + static_cast<size_t>(row) * V + mytok)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float own = inb ? quad_sum(v, mr, kh, kl) : 0.f;
+            ct.quads[lane] = own;
+            __syncwarp();
             float p = 0.f;
-            if (tk < 0 || tk >= V) {
-                a.status[b] = DDT_E_BADINPUT;
-            } else if (rflag == 0) {
-                if (greedy) {
-                    p = tk == idx ? 1.f : 0.f;
-                } else {
-                    const float x = a.logits[static_cast<size_t>(row) * V + tk];
-                    p = __fdiv_rn(weight(x, ct.row_m, kh, kl), ct.row_s);
-                }
+            for (int k = 0; k < R; ++k) {
+                const float qv = ct.quads[k];
+                if (k <= lane) p = __fadd_rn(p, qv);
             }
-            a.node_p[tb + c] = p;
+            const int kst = choose(__ballot_sync(full, own > 0.f && p > tl), __ballot_sync(full, own > 0.f));
+            const float before = __shfl_sync(full, p, kst > 0 ? kst - 1 : 0);
+            const float tk = __fsub_rn(tl, kst > 0 ? before : 0.f);
+            if (lane == kst) {
+                // element: the float4's own partial sums
+                const float e[4] = {weight(v.x, mr, kh, kl), weight(v.y, mr, kh, kl), weight(v.z, mr, kh, kl),
+                                    weight(v.w, mr, kh, kl)};
+                float acc = 0.f;
+                int pick = -1, lastpos = 0;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    acc = jj == 0 ? e[0] : __fadd_rn(acc, e[jj]);
+                    if (e[jj] > 0.f) {
+                        lastpos = jj;
+                        if (pick < 0 && acc > tk) pick = jj;
+                    }
+                }
+                a.sample_tok[row] = static_cast<int>(mytok) + (pick >= 0 ? pick : lastpos);
+            }
         }
+
+        // ---- greedy result, flagged rows, node probabilities (rank 0)
+        if (rank == 0) {
+            const int idx = ct.row_idx == INT_MAX ? 0 : ct.row_idx;
+            if (threadIdx.x == 0) {
+                if (rflag != 0) {
+                    a.sample_tok[row] = -1;
+                    a.status[b] = (rflag & kFlagTimeout) ? DDT_E_TIMEOUT : DDT_E_BADINPUT;
+                } else if (kGreedy) {
+                    a.sample_tok[row] = idx;
+                }
+                if (i == 0) a.node_p[tb] = 1.f;
+            }
+            if (child) {
+                float p = 0.f;
+                if (!tok_ok) {
+                    a.status[b] = DDT_E_BADINPUT;
+                } else if (rflag == 0) {
+                    p = kGreedy ? (c_tok == idx ? 1.f : 0.f) : __fdiv_rn(exp2_diff(c_x, ct.row_m, kh, kl), ct.row_s);
+                }
+                a.node_p[tb + c] = p;
+            }
+        }
+        parity ^= 1;
+        __syncthreads();  // the next row overwrites the region summaries
     }
-    cluster_wait();  // no CTA leaves while another may still read its summary
+    cluster_sync();  // no CTA leaves while another may still read its summary
+}
+
+size_t smem_bytes(int R, int nreg) {
+    return static_cast<size_t>(kWarps * kStages * R * 128 + nreg * 32) * 4 + sizeof(Ctrl);
 }
 
 }  // namespace
 
 SamplePlan plan_sample(int V, long long rows, int sms, int max_cluster) {
-    SamplePlan p{0, 0, 0};
-    if (V < 4 || (V & 3) || rows < 1) return p;
-    int C = 1;
-    // about 20K tokens (80 KB) per CTA; more CTAs when few rows would leave SMs idle
-    while (C < max_cluster && static_cast<long long>(C) * 20480 < V) C <<= 1;
-    while (C < max_cluster && rows * C < sms && static_cast<long long>(C) * 2048 <= V) C <<= 1;
-    int r = static_cast<int>((V + C * 1024LL - 1) / (C * 1024LL));
-    while (r > kSampleMaxRows && C < max_cluster) {
-        C <<= 1;
-        r = static_cast<int>((V + C * 1024LL - 1) / (C * 1024LL));
+    SamplePlan p{};
+    if (V < 4 || (V & 3) || rows < 1 || rows >= (1LL << 31)) return p;
+    // Pick C for the shortest makespan: rows go round-robin over the G = 2 *
+    // sms / C clusters that fit at once (two CTAs per SM); a round costs a
+    // CTA its share of a row plus the row's fixed synchronisation, counted as
+    // the streaming time of about 60 (one CTA) or 120 (a cluster: barrier and
+    // exchange on top) 128-token rows. Ties go to the smaller C.
+    const long long slots = 2LL * sms;
+    double best = 0.0;
+    for (int C = 1; C <= max_cluster; C <<= 1) {
+        const long long per_cta = (V + C - 1) / C;  // tokens
+        if (C > 1 && per_cta < 2048) break;         // too little of a row to split further
+        const long long rows128 = (per_cta + 127) / 128;
+        // region shape: R odd, 8..128 regions (a multiple of 8); the least
+        // capacity past the CTA's share, slightly preferring longer regions
+        int bR = 0, bN = 0;
+        double bscore = 0.0;
+        for (int R = kSampleMaxRows; R >= 1; R -= 2) {
+            const long long nreg = (rows128 + 8LL * R - 1) / (8LL * R) * 8;
+            if (nreg > kSampleMaxRegions) continue;
+            const double score = static_cast<double>(nreg * R) * (1.0 + 0.01 * (kSampleMaxRows - R));
+            if (bR == 0 || score < bscore) {
+                bscore = score;
+                bR = R;
+                bN = static_cast<int>(nreg);
+            }
+        }
+        if (bR == 0) continue;
+        const long long G = slots / C > 0 ? slots / C : 1;
+        const double t = static_cast<double>((rows + G - 1) / G) * static_cast<double>(bN * bR + (C > 1 ? 120 : 60));
+        if (p.C == 0 || t < best * 0.999) {
+            best = t;
+            p.C = C;
+            p.R = bR;
+            p.nreg = bN;
+        }
     }
-    if (r > kSampleMaxRows || rows * C >= (1LL << 31)) return p;
-    p.C = C;
-    p.r = r;
-    p.smem = static_cast<size_t>(r) * 5120 + sizeof(Ctrl);
+    if (p.C != 0) p.smem = smem_bytes(p.R, p.nreg);
     return p;
 }
 
@@ -494,21 +673,25 @@ int sample_max_cluster() {
     static std::once_flag once;
     static int max_c = 0;
     std::call_once(once, [] {
-        const size_t smem_max = static_cast<size_t>(kSampleMaxRows) * 5120 + sizeof(Ctrl);
-        if (cudaFuncSetAttribute(tree_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem_max)) != cudaSuccess)
+        const int smem_max = static_cast<int>(smem_bytes(kSampleMaxRows, kSampleMaxRegions));
+        if (cudaFuncSetAttribute(tree_sample_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(tree_sample_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
+                cudaSuccess)
             return;
         max_c = 8;
-        if (cudaFuncSetAttribute(tree_sample_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess) {
+        if (cudaFuncSetAttribute(tree_sample_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(tree_sample_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                cudaSuccess) {
             cudaGetLastError();
             return;
         }
-        // a cluster of 16 CTAs of the largest size this library launches
+        // a cluster of 16 CTAs of the size the 16-CTA plans use
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(16);
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = static_cast<size_t>(10) * 5120 + sizeof(Ctrl);
+        cfg.dynamicSmemBytes = smem_bytes(kSampleMaxRows, 16);
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 16;
@@ -517,7 +700,7 @@ int sample_max_cluster() {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, tree_sample_kernel, &cfg) == cudaSuccess && n > 0) max_c = 16;
+        if (cudaOccupancyMaxActiveClusters(&n, tree_sample_kernel<false>, &cfg) == cudaSuccess && n > 0) max_c = 16;
         cudaGetLastError();
     });
     return max_c;
@@ -525,22 +708,9 @@ int sample_max_cluster() {
 
 cudaError_t launch_tree_sample(const ddt_tree &tree, const float *logits, int V, double kd, const float *u01,
                                int32_t *sample_tok, float *node_p, const SamplePlan &plan, cudaStream_t s) {
-    SampleArgs a{};
-    a.logits = logits;
-    a.u01 = u01;
-    a.token = tree.token;
-    a.parent = tree.parent;
-    a.n_nodes = tree.n_nodes;
-    a.sample_tok = sample_tok;
-    a.node_p = node_p;
-    a.status = tree.status;
-    a.kd = kd;
-    a.Qc = tree.Qc;
-    a.V = V;
-    a.C = plan.C;
-    a.r = plan.r;
+    const bool greedy = kd == 0.0;
+    void (*kernel)(SampleArgs) = greedy ? tree_sample_kernel<true> : tree_sample_kernel<false>;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(tree.B) * tree.Qc * plan.C));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = s;
@@ -551,7 +721,62 @@ cudaError_t launch_tree_sample(const ddt_tree &tree, const float *logits, int V,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tree_sample_kernel, a);
+    // as many clusters as fit on the device at once (a persistent grid), at
+    // most one per row; the occupancy answer is cached per shape
+    static std::mutex mu;
+    static int cached_c = 0, cached_g = 0, cached_dev = -1;
+    static size_t cached_smem = 0;
+    int dev = 0, G = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cached_c == plan.C && cached_smem == plan.smem && cached_dev == dev) {
+            G = cached_g;
+        } else {
+            cfg.gridDim = dim3(static_cast<unsigned>(plan.C));
+            if (cudaOccupancyMaxActiveClusters(&G, tree_sample_kernel<false>, &cfg) != cudaSuccess || G < 1) {
+                cudaGetLastError();
+                return cudaErrorInvalidConfiguration;
+            }
+            cached_c = plan.C;
+            cached_smem = plan.smem;
+            cached_dev = dev;
+            cached_g = G;
+        }
+    }
+    const long long rows = static_cast<long long>(tree.B) * tree.Qc;
+    SampleArgs a{};
+    a.logits = logits;
+    a.u01 = u01;
+    a.token = tree.token;
+    a.parent = tree.parent;
+    a.n_nodes = tree.n_nodes;
+    a.sample_tok = sample_tok;
+    a.node_p = node_p;
+    a.status = tree.status;
+    if (!greedy) {
+        // kd = kh + kl with kl > 0: kh the largest float below kd
+        float kh = static_cast<float>(kd);
+        if (static_cast<double>(kh) >= kd) kh = nextafterf(kh, 0.f);
+        a.kh = kh;
+        a.kl = static_cast<float>(kd - static_cast<double>(kh));
+    }
+    a.Qc = tree.Qc;
+    a.V = V;
+    a.C = plan.C;
+    a.R = plan.R;
+    a.nreg = plan.nreg;
+    // each launch gives a cluster at most kSampleListCap rows
+    const long long per_launch = static_cast<long long>(G) * kSampleListCap;
+    for (long long r0 = 0; r0 < rows; r0 += per_launch) {
+        const long long r1 = r0 + per_launch < rows ? r0 + per_launch : rows;
+        a.row0 = static_cast<int>(r0);
+        a.rows_end = static_cast<int>(r1);
+        a.G = static_cast<int>(r1 - r0 < G ? r1 - r0 : G);
+        cfg.gridDim = dim3(static_cast<unsigned>(a.G * plan.C));
+        if (cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a)) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace ddt
