@@ -64,7 +64,7 @@ cudaError_t launch_kv_commit(int B, int D, int Tcap, const int32_t *accept_len, 
 // C CTAs per row; each CTA owns nreg regions of 128 R tokens (R odd).
 constexpr int kSampleMaxRows = 11;      // R: float4 per lane in a region
 constexpr int kSampleMaxRegions = 128;  // regions per CTA
-constexpr int kSampleListCap = 256;     // rows per cluster and launch
+constexpr int kSampleListCap = 128;     // rows per cluster and launch
 struct SamplePlan {
     int C;        // CTAs per row (cluster size); 0 = shape not supported
     int R;        // float4 per lane in a region (odd)

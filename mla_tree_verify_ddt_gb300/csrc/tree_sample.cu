@@ -21,9 +21,9 @@
 // Layout of the work. A persistent grid of clusters of C CTAs; cluster g
 // takes rows g, g + G, g + 2G, ... (G clusters). In a row, CTA c owns tokens
 // [c * NREG * R * 128, (c + 1) * NREG * R * 128), cut into NREG regions of
-// 128 R tokens; warp w takes regions w, w + 8, ... and streams them, row
-// after row, through a two-stage ring of bulk copies into shared memory; the
-// logits are read from HBM once. In a region lane l owns the R consecutive
+// 128 R tokens; warp w takes the contiguous regions w Q .. w Q + Q - 1
+// (Q = NREG / 8) and streams them, row after row, through a two-stage ring
+// of bulk copies into shared memory; the logits are read from HBM once. In a region lane l owns the R consecutive
 // float4 l R .. l R + R - 1 (R odd: the 8 lanes of a 128-bit shared-memory
 // phase then hit 8 different bank groups). C is the smallest cluster that
 // still fills the GPU (two CTAs per SM): every row ends with block-wide (and,
@@ -31,21 +31,25 @@
 // row, the smaller that fixed cost against its streaming time.
 //
 // Per region (one warp):
-//   pass 1  largest logit (NaN-propagating max; the greedy kernel tracks the
-//           first index of the largest instead);
+//   pass 1  largest logit (NaN-propagating max; the greedy kernel then finds
+//           its first index);
 //   pass 2  weights against the region's largest logit, 4 at a time (a quad
 //           sum), a sequential sum per lane, an inclusive scan over the
-//           lanes (its last entry is the region total).
+//           lanes (its last entry is the region total); the warp folds the
+//           total into its running float-pair prefix over its regions, kept
+//           in units of its running maximum (a new maximum rescales the
+//           prefix: an exact power of two times a hardware exp2 of the
+//           fraction).
 // Per row:
-//   CTA      the regions' maxima combine into the CTA's, each region's total
-//           is scaled to it (an exact power of two times a hardware exp2 of
-//           the fraction) and scanned over the regions as a float pair;
-//   cluster  every CTA publishes (max, first index, total) in its shared
-//           memory; after a cluster barrier every CTA reads the C summaries
-//           through distributed shared memory and computes the same row
-//           maximum, float-pair scan, total and winning CTA;
-//   locate   the winning CTA descends region -> lane -> float4 -> element over
-//           the sums it built; for the float4 level it reloads the chosen
+//   CTA      the 8 warps' prefixes scaled to the CTA's maximum and scanned in
+//           warp order;
+//   cluster  every CTA writes its (max, first index, total) into every CTA
+//           of the cluster (distributed shared memory stores); after a
+//           cluster barrier each reads the C summaries locally and computes
+//           the same row maximum, float-pair scan, total and winning CTA;
+//   locate   the winning CTA descends warp -> region -> lane -> float4 ->
+//           element over the sums it built (a region's prefix brought to its
+//           warp's final maximum); for the float4 level it reloads the chosen
 //           lane's R float4 from memory and recomputes their quad sums, which
 //           come out bit-identical (one fixed sequence of correctly rounded
 //           operations). A threshold past a level's total takes that level's
@@ -71,21 +75,26 @@ constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kStages = 2;  // ring depth per warp
 constexpr int kFlagNan = 1, kFlagTimeout = 2, kFlagNoDist = 4;
+constexpr int kMaxNodes = DDT_MAX_BUDGET + 1;
 
 struct Ctrl {
     uint64_t bar[kWarps][kStages];
-    float rmax[kSampleMaxRegions];   // region maximum
-    int ridx[kSampleMaxRegions];     // its first index (greedy)
-    int rflag[kSampleMaxRegions];
-    float rtot[kSampleMaxRegions];   // region total, units of 2^((x - rmax) kd)
+    // per region; warp w owns regions w Q .. w Q + Q - 1 (contiguous tokens)
+    float rmax[kSampleMaxRegions];     // region maximum
+    float rtot[kSampleMaxRegions];     // region total, units of 2^((x - rmax) kd)
     unsigned lpos[kSampleMaxRegions];  // lanes of the region with nonzero weight
-    float fscale[kSampleMaxRegions]; // 2^((rmax - m_c) kd)
-    float mass_hi[kSampleMaxRegions], mass_lo[kSampleMaxRegions];  // rtot * fscale
-    float scan_hi[kSampleMaxRegions], scan_lo[kSampleMaxRegions];  // inclusive scan of mass
-    float quads[32];                 // the located lane's quad sums
-    // published to the cluster, double-buffered by row parity
-    float pub_m[2], pub_hi[2], pub_lo[2];
-    int pub_idx[2], pub_flag[2];
+    float rref[kSampleMaxRegions];     // the warp's running maximum W after this region
+    float rp_hi[kSampleMaxRegions], rp_lo[kSampleMaxRegions];  // running prefix, units of 2^((x - W) kd)
+    // per warp: maximum (greedy: its first index), flags, total, and the
+    // CTA-level scale, mass and inclusive scan
+    float wmax[kWarps], wp_hi[kWarps], wp_lo[kWarps];
+    int widx[kWarps], wflag[kWarps];
+    float wfs[kWarps], wmass[kWarps], wscan_hi[kWarps], wscan_lo[kWarps];
+    float quads[32];  // the located lane's quad sums
+    // the cluster's CTA summaries, written by each CTA into every CTA of the
+    // cluster (slot = writer's rank), double-buffered by row parity
+    float xm[2][16], xhi[2][16], xlo[2][16];
+    int xidx[2][16], xflag[2][16];
     // the row's result, identical in every CTA of the cluster
     int row_flag, row_idx, cstar;
     float row_m, row_s, t_hi, t_lo;
@@ -94,6 +103,10 @@ struct Ctrl {
     int wcount[kWarps];
     int list_row[kSampleListCap];
     int list_n[kSampleListCap];
+    float list_u[kSampleListCap];
+    // node i's children (thread c holds node c): parent, token, logit
+    int cpar[kMaxNodes], ctok[kMaxNodes];
+    float cx[kMaxNodes];
 };
 
 struct SampleArgs {
@@ -107,7 +120,7 @@ struct SampleArgs {
     int32_t *status;
     float kh, kl;        // log2(e) / temperature = kh + kl, kl > 0 (unused by the greedy kernel)
     int row0, rows_end;  // this launch's rows: cluster g takes row0 + g + t * G < rows_end
-    int Qc, V, C, R, nreg, G;
+    int Qc, V, C, nreg, G;
 };
 
 // Bulk copy global -> this CTA's shared memory, credited to `bar`.
@@ -118,15 +131,24 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  : "memory");
 }
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-    return v;
+// Store into the same shared-memory location of CTA `rank` of the cluster.
+__device__ __forceinline__ void st_peer_f32(float *p, uint32_t rank, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(mapa_shared(smem_u32(p), rank)), "f"(v) : "memory");
 }
-__device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
-    int v;
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-    return v;
+__device__ __forceinline__ void st_peer_s32(int *p, uint32_t rank, int v) {
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(mapa_shared(smem_u32(p), rank)), "r"(v) : "memory");
+}
+
+// 4 bytes global -> shared without holding a register; cp.async.wait_all
+// makes them visible to the issuing thread.
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 
 // max that returns NaN when either operand is NaN
@@ -176,7 +198,12 @@ __device__ __forceinline__ float exp2_diff(float a, float b, float kh, float kl)
     const float rest = __fadd_rn(pl, __fadd_rn(__fmul_rn(s, kl), __fmul_rn(err, kh)));
     const float n = rintf(ph);
     const float frac = __fadd_rn(__fsub_rn(ph, n), rest);
-    return ldexpf(ex2_approx(frac), static_cast<int>(n));
+    // times 2^n, -251 <= n <= 0, as products with exact powers of two built
+    // from their bits (2^n = 2^(n + 126) 2^-126 below the normal range)
+    const int ni = static_cast<int>(n);
+    const float r = ex2_approx(frac);
+    return ni >= -126 ? __fmul_rn(r, __int_as_float((ni + 127) << 23))
+                      : __fmul_rn(__fmul_rn(r, __int_as_float((ni + 253) << 23)), __int_as_float(1 << 23));
 }
 
 // ---- float pairs (hi + lo, |lo| <= ulp(hi) / 2): sums of up to a few
@@ -199,10 +226,14 @@ __device__ __forceinline__ ff ff_mul(ff a, float f) {
     const float p = __fmul_rn(a.hi, f);
     return ff_norm(p, __fmaf_rn(a.lo, f, __fmaf_rn(a.hi, f, -p)));
 }
+// a / f: the quotient from the hardware reciprocal, then one correction
+// step with the exact remainder (f > 0; below 2^-100 the plain division,
+// where the reciprocal would overflow or flush)
 __device__ __forceinline__ ff ff_div(ff a, float f) {
-    const float q1 = __fdiv_rn(a.hi, f);
-    const float r = __fadd_rn(__fmaf_rn(-q1, f, a.hi), a.lo);
-    return ff_norm(q1, __fdiv_rn(r, f));
+    const float r = f < 7.9e-31f ? 0.f : rcp_approx(f);
+    const float q1 = f < 7.9e-31f ? __fdiv_rn(a.hi, f) : __fmul_rn(a.hi, r);
+    const float rem = __fadd_rn(__fmaf_rn(-q1, f, a.hi), a.lo);
+    return ff_norm(q1, f < 7.9e-31f ? __fdiv_rn(rem, f) : __fmul_rn(rem, r));
 }
 __device__ __forceinline__ bool ff_gt(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
 __device__ __forceinline__ ff ff_shfl(ff a, int src) {
@@ -226,14 +257,6 @@ __device__ __forceinline__ float warp_scan(float v, int lane) {
         if (lane >= o) v = __fadd_rn(u, v);
     }
     return v;
-}
-
-__device__ __forceinline__ void consider(float x, int j, float &best, int &bidx, int &flag) {
-    if (x != x) flag |= kFlagNan;
-    else if (x > best) {
-        best = x;
-        bidx = j;
-    }
 }
 
 // Larger value, or the lower index among equal values; flags OR-ed; the
@@ -264,10 +287,13 @@ __device__ __forceinline__ int node_count(const SampleArgs &a, int b) {
     return n < 1 ? 1 : (n > a.Qc ? a.Qc : n);
 }
 
-template <bool kGreedy>
+// R (float4 per lane in a region) is a template parameter so that the
+// region passes unroll: every load and exp2 of a lane's run can be in flight
+// at once.
+template <bool kGreedy, int R>
 __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    const int C = a.C, V = a.V, Qc = a.Qc, R = a.R, NREG = a.nreg, G = a.G;
+    const int C = a.C, V = a.V, Qc = a.Qc, NREG = a.nreg, G = a.G;
     const int Q = NREG / kWarps;  // regions per warp per row
     const int g = blockIdx.x / C;
     const int rank = static_cast<int>(cluster_ctarank());
@@ -285,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
         mbar_fence_init();
     }
     // ---- the cluster's rows that hold a node, compacted in order (every CTA
-    // of the cluster builds the same list); padding slots get their outputs here
+    // of the cluster builds the same list); padding slots get their outputs
+    // here; each row's uniform is fetched now, not at the end of the row
     {
         const int span = (a.rows_end - a.row0 - g + G - 1) / G;
         int base = 0;
@@ -294,10 +321,12 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
             const int row = a.row0 + g + t * G;
             bool valid = false;
             int n = 0;
+            float u = 0.f;
             if (t < span) {
                 const int b = row / Qc;
                 n = node_count(a, b);
                 valid = row - b * Qc < n;
+                if (!kGreedy && valid) u = a.u01[row];
                 if (!valid && rank == 0) {
                     a.sample_tok[row] = -1;
                     a.node_p[row] = 0.f;
@@ -312,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
                 const int pos = off + __popc(bal & ((1u << lane) - 1u));
                 ct.list_row[pos] = row;
                 ct.list_n[pos] = n;
+                ct.list_u[pos] = u;
             }
             for (int w = 0; w < kWarps; ++w) base += ct.wcount[w];
             __syncthreads();
@@ -330,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
         const int prow = ct.list_row[pl];
         const int stage = static_cast<int>(issued & 1u);
         const uint32_t bar = smem_u32(&ct.bar[warp][stage]);
-        const long long reg0 = cta0 + static_cast<long long>(warp + kWarps * pq) * rtok;
+        const long long reg0 = cta0 + static_cast<long long>(warp * Q + pq) * rtok;
         const long long left = static_cast<long long>(V) - reg0;
         const int nvalid = left <= 0 ? 0 : (left >= rtok ? rtok : static_cast<int>(left));
         if (nvalid > 0) {
@@ -351,6 +381,8 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
         issue();
     }
     __syncwarp();
+    // every CTA of the cluster is running before any writes into another
+    if (C > 1) cluster_sync();
 
     uint32_t used = 0;  // regions consumed by this warp
     int parity = 0;     // row count parity (publication buffer)
@@ -358,132 +390,155 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
         const int row = ct.list_row[li], n = ct.list_n[li];
         const int b = row / Qc, i = row - b * Qc;
         const size_t tb = static_cast<size_t>(b) * Qc;
-        // loads the end of the row needs, issued now so they land during the
-        // region passes: the uniform (warp 0), the children of node i (rank 0)
-        const float u = (!kGreedy && warp == 0) ? a.u01[row] : 0.f;
+        // what the end of the row needs from memory is copied into shared
+        // memory while the regions stream (a load left for the end of the row
+        // would queue behind the other CTAs' streams): node i's children,
+        // their tokens, then (once the tokens are in) their logits (rank 0)
+        const float u = ct.list_u[li];
         const int c = threadIdx.x;
-        int c_par = -1, c_tok = -1;
-        if (rank == 0 && c >= 1 && c < n) {
-            c_par = a.parent[tb + c];
-            c_tok = a.token[tb + c];
+        const bool cslot = rank == 0 && c >= 1 && c < n;
+        if (cslot) {
+            cp_async_4(&ct.cpar[c], a.parent + tb + c);
+            cp_async_4(&ct.ctok[c], a.token + tb + c);
         }
+        bool child = false, tok_ok = false;
+        int c_tok = -1;
 
-        // ---- this warp's regions of the row
+        // ---- this warp's regions of the row, in token order: a running
+        // maximum W and (sampling) a running float-pair prefix P of the
+        // regions' totals in units of 2^((x - W) kd)
+        float W = -INFINITY;
+        int widx = INT_MAX, wflag = 0;
+        ff P = {0.f, 0.f};
         for (int q = 0; q < Q; ++q) {
-            const int j = warp + kWarps * q;
+            const int j = warp * Q + q;
             const int stage = static_cast<int>(used & 1u);
             const long long reg0 = cta0 + static_cast<long long>(j) * rtok;
             const long long left = static_cast<long long>(V) - reg0;
             const int nq = (left <= 0 ? 0 : (left >= rtok ? rtok : static_cast<int>(left))) >> 2;
             int flag = 0;
             if (!wait_bar(smem_u32(&ct.bar[warp][stage]), (used >> 1) & 1u)) flag |= kFlagTimeout;
+            // the lane's run into registers (past V: -inf, weight 0), then the
+            // stage goes straight back to the producer
             const int q0 = lane * R;  // this lane's first float4 of the region
             const float4 *reg4 = reinterpret_cast<const float4 *>(stages + (warp * kStages + stage) * rtok) + q0;
-            float best = -INFINITY;
-            int bidx = INT_MAX;
-            float tot = 0.f;
-            if (kGreedy) {
-                if (!(flag & kFlagTimeout)) {
-                    for (int k = 0; k < R; ++k) {
-                        if (q0 + k < nq) {
-                            const float4 v = reg4[k];
-                            const int t = static_cast<int>(reg0) + 4 * (q0 + k);
-                            consider(v.x, t, best, bidx, flag);
-                            consider(v.y, t + 1, best, bidx, flag);
-                            consider(v.z, t + 2, best, bidx, flag);
-                            consider(v.w, t + 3, best, bidx, flag);
-                        }
-                    }
-                }
-                warp_argmax(best, bidx, flag);
-            } else {
-                // pass 1: NaN-propagating max
-                if (!(flag & kFlagTimeout)) {
-                    for (int k = 0; k < R; ++k) {
-                        if (q0 + k < nq) {
-                            const float4 v = reg4[k];
-                            best = max_nan(max_nan(best, v.x), max_nan(v.y, max_nan(v.z, v.w)));
-                        }
-                    }
-                }
+            float4 x[R];
 #pragma unroll
-                for (int o = 16; o; o >>= 1) {
-                    best = max_nan(best, __shfl_xor_sync(full, best, o));
-                    flag |= __shfl_xor_sync(full, flag, o);
+            for (int k = 0; k < R; ++k)
+                x[k] = (q0 + k < nq && !(flag & kFlagTimeout)) ? reg4[k]
+                                                               : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            __syncwarp();  // every lane has its run
+            ++used;
+            if (lane == 0) issue();
+            if (q == 0 && cslot) {
+                cp_async_wait_all();
+                child = ct.cpar[c] == i;
+                c_tok = ct.ctok[c];
+                tok_ok = c_tok >= 0 && c_tok < V;
+                if (child && tok_ok && !kGreedy) cp_async_4(&ct.cx[c], a.logits + static_cast<size_t>(row) * V + c_tok);
+            }
+            // region maximum (NaN-propagating)
+            float best = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < R; ++k)
+                best = max_nan(best, max_nan(max_nan(x[k].x, x[k].y), max_nan(x[k].z, x[k].w)));
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                best = max_nan(best, __shfl_xor_sync(full, best, o));
+                flag |= __shfl_xor_sync(full, flag, o);
+            }
+            if (best != best) flag |= kFlagNan;
+            if (!kGreedy && best == INFINITY) flag |= kFlagNoDist;
+            wflag |= flag;
+            if (kGreedy) {
+                // its first index: the lanes' first element equal to it, lowest lane
+                int bidx = INT_MAX;
+#pragma unroll
+                for (int k = R - 1; k >= 0; --k) {
+                    const int t = static_cast<int>(reg0) + 4 * (q0 + k);
+                    bidx = x[k].w == best ? t + 3 : bidx;
+                    bidx = x[k].z == best ? t + 2 : bidx;
+                    bidx = x[k].y == best ? t + 1 : bidx;
+                    bidx = x[k].x == best ? t : bidx;
                 }
-                if (best != best) flag |= kFlagNan;
-                // pass 2: quad sums, a sequential sum per lane, a scan over lanes
-                if (flag == 0 && best > -INFINITY && best < INFINITY) {
+                bidx = static_cast<int>(__reduce_min_sync(full, static_cast<unsigned>(bidx)));
+                if (best > W || (best == W && bidx < widx)) {
+                    W = best;
+                    widx = bidx;
+                }
+            } else {
+                // weights: quad sums, a sequential sum per lane, a scan over lanes
+                float tot = 0.f;
+                if (wflag == 0 && best > -INFINITY) {
+                    float qs[R];
+#pragma unroll
+                    for (int k = 0; k < R; ++k) qs[k] = quad_sum(x[k], best, kh, kl);
                     float s = 0.f;
-                    for (int k = 0; k < R; ++k)
-                        if (q0 + k < nq) s = __fadd_rn(s, quad_sum(reg4[k], best, kh, kl));
+#pragma unroll
+                    for (int k = 0; k < R; ++k) s = __fadd_rn(s, qs[k]);
                     const float inc = warp_scan(s, lane);
                     lscan[j * 32 + lane] = inc;
                     const unsigned lp = __ballot_sync(full, s > 0.f);
                     if (lane == 0) ct.lpos[j] = lp;
                     tot = __shfl_sync(full, inc, 31);
+                    // into the running prefix (a new maximum rescales it first)
+                    if (best > W) {
+                        P = ff_mul(P, exp2_diff(W, best, kh, kl));
+                        W = best;
+                    }
+                    P = ff_add(P, ff_mul({tot, 0.f}, exp2_diff(best, W, kh, kl)));
+                }
+                if (lane == 0) {
+                    ct.rmax[j] = best;
+                    ct.rtot[j] = tot;
+                    ct.rref[j] = W;
+                    ct.rp_hi[j] = P.hi;
+                    ct.rp_lo[j] = P.lo;
                 }
             }
-            if (lane == 0) {
-                ct.rmax[j] = best;
-                ct.ridx[j] = bidx;
-                ct.rflag[j] = flag;
-                ct.rtot[j] = tot;
-            }
-            __syncwarp();  // every lane is done with the stage
-            ++used;
-            if (lane == 0) issue();
         }
-        // the child's logit (used after the exchange)
-        const bool child = c_par == i;
-        const bool tok_ok = c_tok >= 0 && c_tok < V;
-        const float c_x = (child && tok_ok && !kGreedy) ? a.logits[static_cast<size_t>(row) * V + c_tok] : 0.f;
+        if (lane == 0) {
+            ct.wmax[warp] = W;
+            ct.widx[warp] = widx;
+            ct.wflag[warp] = wflag;
+            ct.wp_hi[warp] = P.hi;
+            ct.wp_lo[warp] = P.lo;
+        }
         __syncthreads();
 
-        // ---- CTA summary (warp 0)
+        // ---- CTA summary (warp 0): the 8 warps' maxima, their totals scaled
+        // to the CTA's maximum and scanned in warp (token) order
         if (warp == 0) {
-            float m = -INFINITY;
-            int idx = INT_MAX, f = 0;
-            for (int j = lane; j < NREG; j += 32) {  // regions in token order
-                const float v = ct.rmax[j];
-                const int ix = ct.ridx[j];
-                f |= ct.rflag[j];
-                if (v > m || (v == m && ix < idx)) {
-                    m = v;
-                    idx = ix;
-                }
-            }
+            const bool wl = lane < kWarps;
+            float m = wl ? ct.wmax[lane] : -INFINITY;
+            int idx = wl ? ct.widx[lane] : INT_MAX;
+            int f = wl ? ct.wflag[lane] : 0;
+            const float wm = m;
             warp_argmax(m, idx, f);
             ff total = {0.f, 0.f};
-            if (!kGreedy && f == 0 && m > -INFINITY && m < INFINITY) {
-                for (int j0 = 0; j0 < NREG; j0 += 32) {
-                    const int j = j0 + lane;
-                    float fs = 0.f;
-                    ff mass = {0.f, 0.f};
-                    if (j < NREG) {
-                        fs = exp2_diff(ct.rmax[j], m, kh, kl);
-                        mass = ff_mul({ct.rtot[j], 0.f}, fs);
-                    }
-                    const ff sc = ff_add(total, ff_scan(mass, lane));
-                    if (j < NREG) {
-                        ct.fscale[j] = fs;
-                        ct.mass_hi[j] = mass.hi;
-                        ct.mass_lo[j] = mass.lo;
-                        ct.scan_hi[j] = sc.hi;
-                        ct.scan_lo[j] = sc.lo;
-                    }
-                    total = ff_shfl(sc, 31);
+            if (!kGreedy && f == 0 && m > -INFINITY) {
+                const float fs = wl ? exp2_diff(wm, m, kh, kl) : 0.f;
+                const ff mass = wl ? ff_mul({ct.wp_hi[lane], ct.wp_lo[lane]}, fs) : ff{0.f, 0.f};
+                const ff sc = ff_scan(mass, lane);
+                if (wl) {
+                    ct.wfs[lane] = fs;
+                    ct.wmass[lane] = mass.hi;
+                    ct.wscan_hi[lane] = sc.hi;
+                    ct.wscan_lo[lane] = sc.lo;
                 }
+                total = ff_shfl(sc, 31);
             }
-            if (lane == 0) {
-                ct.pub_m[parity] = m;
-                ct.pub_idx[parity] = idx;
-                ct.pub_flag[parity] = f;
-                ct.pub_hi[parity] = total.hi;
-                ct.pub_lo[parity] = total.lo;
+            // the CTA's summary into every CTA of the cluster
+            if (lane < C) {
+                st_peer_f32(&ct.xm[parity][rank], lane, m);
+                st_peer_f32(&ct.xhi[parity][rank], lane, total.hi);
+                st_peer_f32(&ct.xlo[parity][rank], lane, total.lo);
+                st_peer_s32(&ct.xidx[parity][rank], lane, idx);
+                st_peer_s32(&ct.xflag[parity][rank], lane, f);
             }
         }
-        cluster_sync();
+        if (C > 1) cluster_sync();
+        else __syncthreads();
 
         // ---- cluster exchange (warp 0 of every CTA computes the same result)
         if (warp == 0) {
@@ -491,11 +546,10 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
             ff ps = {0.f, 0.f};
             int pi = INT_MAX, pf = 0;
             if (lane < C) {
-                pm = ld_cluster_f32(mapa_shared(smem_u32(&ct.pub_m[parity]), lane));
-                ps.hi = ld_cluster_f32(mapa_shared(smem_u32(&ct.pub_hi[parity]), lane));
-                ps.lo = ld_cluster_f32(mapa_shared(smem_u32(&ct.pub_lo[parity]), lane));
-                pi = ld_cluster_s32(mapa_shared(smem_u32(&ct.pub_idx[parity]), lane));
-                pf = ld_cluster_s32(mapa_shared(smem_u32(&ct.pub_flag[parity]), lane));
+                pm = ct.xm[parity][lane];
+                ps = {ct.xhi[parity][lane], ct.xlo[parity][lane]};
+                pi = ct.xidx[parity][lane];
+                pf = ct.xflag[parity][lane];
             }
             float M = pm;
             int idx = pi, f = pf;
@@ -530,24 +584,26 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
         // ---- locate the sample inside the winning CTA (warp 0)
         if (!kGreedy && rflag == 0 && rank == ct.cstar && warp == 0) {
             const ff tc = {ct.t_hi, ct.t_lo};
-            // region: first of positive mass whose scan passes tc, else the
-            // last of positive mass
-            int jst = -1, jlast = 0;
-            for (int j0 = 0; j0 < NREG; j0 += 32) {
-                const int j = j0 + lane;
-                const bool pos = j < NREG && ct.mass_hi[j] > 0.f;
-                const unsigned pick = __ballot_sync(full, pos && ff_gt({ct.scan_hi[j], ct.scan_lo[j]}, tc));
-                const unsigned any = __ballot_sync(full, pos);
-                if (pick) {
-                    jst = j0 + __ffs(pick) - 1;
-                    break;
-                }
-                if (any) jlast = j0 + 31 - __clz(any);
-            }
-            if (jst < 0) jst = jlast;
-            const ff pre_j = jst > 0 ? ff{ct.scan_hi[jst - 1], ct.scan_lo[jst - 1]} : ff{0.f, 0.f};
-            const ff tjf = ff_div(ff_add(tc, ff_neg(pre_j)), ct.fscale[jst]);
-            const float tj = __fadd_rn(tjf.hi, tjf.lo);
+            // warp: first of positive mass whose scan passes tc, else the last
+            // of positive mass
+            const bool wpos = lane < kWarps && ct.wmass[lane] > 0.f;
+            const bool wpick = wpos && ff_gt({ct.wscan_hi[lane], ct.wscan_lo[lane]}, tc);
+            const int wst = choose(__ballot_sync(full, wpick), __ballot_sync(full, wpos));
+            const ff pre_w = wst > 0 ? ff{ct.wscan_hi[wst - 1], ct.wscan_lo[wst - 1]} : ff{0.f, 0.f};
+            const ff tw = ff_div(ff_add(tc, ff_neg(pre_w)), ct.wfs[wst]);  // units of 2^((x - W) kd)
+            const float Ww = ct.wmax[wst];
+            // region of the warp: its running prefix, brought to the warp's
+            // final maximum
+            const int j = wst * Q + lane;
+            const bool rl = lane < Q;
+            const bool rpos = rl && ct.rtot[j] > 0.f;
+            const ff pconv = rl ? ff_mul({ct.rp_hi[j], ct.rp_lo[j]}, exp2_diff(ct.rref[j], Ww, kh, kl)) : ff{0.f, 0.f};
+            const int qst = choose(__ballot_sync(full, rpos && ff_gt(pconv, tw)), __ballot_sync(full, rpos));
+            const ff pre_q = qst > 0 ? ff_shfl(pconv, qst - 1) : ff{0.f, 0.f};
+            const int jst = wst * Q + qst;
+            const float mr = ct.rmax[jst];
+            const ff tjf = ff_div(ff_add(tw, ff_neg(qst > 0 ? pre_q : ff{0.f, 0.f})), exp2_diff(mr, Ww, kh, kl));
+            const float tj = __fadd_rn(tjf.hi, tjf.lo);  // units of 2^((x - rmax) kd)
             // lane: the region's lane scan, among the lanes of nonzero weight
             // (the scan's fixed tree need not rise by an empty lane's zero)
             const float inc = lscan[jst * 32 + lane];
@@ -558,7 +614,6 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
             // float4 of the lane: its quad sums again, from the logits in
             // memory, and their sequential prefix (the sequence that made the
             // lane sum)
-            const float mr = ct.rmax[jst];
             const long long ltok0 = cta0 + static_cast<long long>(jst) * rtok + 4LL * lst * R;
             const long long mytok = ltok0 + 4LL * lane;
             const bool inb = lane < R && mytok + 4 <= V;
@@ -568,6 +623,7 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
             ct.quads[lane] = own;
             __syncwarp();
             float p = 0.f;
+#pragma unroll
             for (int k = 0; k < R; ++k) {
                 const float qv = ct.quads[k];
                 if (k <= lane) p = __fadd_rn(p, qv);
@@ -606,11 +662,13 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
                 if (i == 0) a.node_p[tb] = 1.f;
             }
             if (child) {
+                cp_async_wait_all();
+                const float c_x = ct.cx[c];
                 float p = 0.f;
                 if (!tok_ok) {
                     a.status[b] = DDT_E_BADINPUT;
                 } else if (rflag == 0) {
-                    p = kGreedy ? (c_tok == idx ? 1.f : 0.f) : __fdiv_rn(exp2_diff(c_x, ct.row_m, kh, kl), ct.row_s);
+                    p = kGreedy ? (c_tok == idx ? 1.f : 0.f) : __fdividef(exp2_diff(c_x, ct.row_m, kh, kl), ct.row_s);
                 }
                 a.node_p[tb + c] = p;
             }
@@ -618,7 +676,8 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
         parity ^= 1;
         __syncthreads();  // the next row overwrites the region summaries
     }
-    cluster_sync();  // no CTA leaves while another may still read its summary
+    // (no CTA touches another's shared memory after a row's cluster barrier,
+    // so a CTA may leave as soon as its last row is done)
 }
 
 size_t smem_bytes(int R, int nreg) {
@@ -669,24 +728,33 @@ SamplePlan plan_sample(int V, long long rows, int sms, int max_cluster) {
     return p;
 }
 
+namespace {
+using SampleKernel = void (*)(SampleArgs);
+// [greedy][R / 2] for R = 1, 3, ..., kSampleMaxRows
+const SampleKernel kKernels[2][6] = {
+    {tree_sample_kernel<false, 1>, tree_sample_kernel<false, 3>, tree_sample_kernel<false, 5>,
+     tree_sample_kernel<false, 7>, tree_sample_kernel<false, 9>, tree_sample_kernel<false, 11>},
+    {tree_sample_kernel<true, 1>, tree_sample_kernel<true, 3>, tree_sample_kernel<true, 5>,
+     tree_sample_kernel<true, 7>, tree_sample_kernel<true, 9>, tree_sample_kernel<true, 11>}};
+static_assert(kSampleMaxRows == 11, "one kernel per odd R up to kSampleMaxRows");
+}  // namespace
+
 int sample_max_cluster() {
     static std::once_flag once;
     static int max_c = 0;
     std::call_once(once, [] {
         const int smem_max = static_cast<int>(smem_bytes(kSampleMaxRows, kSampleMaxRegions));
-        if (cudaFuncSetAttribute(tree_sample_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(tree_sample_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
-                cudaSuccess)
-            return;
+        for (auto &row : kKernels)
+            for (SampleKernel k : row)
+                if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess)
+                    return;
         max_c = 8;
-        if (cudaFuncSetAttribute(tree_sample_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(tree_sample_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                cudaSuccess) {
-            cudaGetLastError();
-            return;
-        }
+        for (auto &row : kKernels)
+            for (SampleKernel k : row)
+                if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+                    cudaGetLastError();
+                    return;
+                }
         // a cluster of 16 CTAs of the size the 16-CTA plans use
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(16);
@@ -700,7 +768,8 @@ int sample_max_cluster() {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, tree_sample_kernel<false>, &cfg) == cudaSuccess && n > 0) max_c = 16;
+        if (cudaOccupancyMaxActiveClusters(&n, kKernels[0][kSampleMaxRows / 2], &cfg) == cudaSuccess && n > 0)
+            max_c = 16;
         cudaGetLastError();
     });
     return max_c;
@@ -709,7 +778,8 @@ int sample_max_cluster() {
 cudaError_t launch_tree_sample(const ddt_tree &tree, const float *logits, int V, double kd, const float *u01,
                                int32_t *sample_tok, float *node_p, const SamplePlan &plan, cudaStream_t s) {
     const bool greedy = kd == 0.0;
-    void (*kernel)(SampleArgs) = greedy ? tree_sample_kernel<true> : tree_sample_kernel<false>;
+    if (plan.R < 1 || plan.R > kSampleMaxRows || !(plan.R & 1)) return cudaErrorInvalidValue;
+    const SampleKernel kernel = kKernels[greedy ? 1 : 0][plan.R / 2];
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = plan.smem;
@@ -734,7 +804,7 @@ cudaError_t launch_tree_sample(const ddt_tree &tree, const float *logits, int V,
             G = cached_g;
         } else {
             cfg.gridDim = dim3(static_cast<unsigned>(plan.C));
-            if (cudaOccupancyMaxActiveClusters(&G, tree_sample_kernel<false>, &cfg) != cudaSuccess || G < 1) {
+            if (cudaOccupancyMaxActiveClusters(&G, kKernels[0][plan.R / 2], &cfg) != cudaSuccess || G < 1) {
                 cudaGetLastError();
                 return cudaErrorInvalidConfiguration;
             }
@@ -764,7 +834,6 @@ cudaError_t launch_tree_sample(const ddt_tree &tree, const float *logits, int V,
     a.Qc = tree.Qc;
     a.V = V;
     a.C = plan.C;
-    a.R = plan.R;
     a.nreg = plan.nreg;
     // each launch gives a cluster at most kSampleListCap rows
     const long long per_launch = static_cast<long long>(G) * kSampleListCap;
