@@ -252,6 +252,55 @@ def config_dict(wl, inp):
             "l2": "flushed before every timed step (256 MiB write)", "seed": synth.SEED_BASE}
 
 
+def sample_leg(ddtree, wl_idx, wl, inp, depth, n_nodes, tree, s, flush, dev, n, torch):
+    """ddt_tree_sample at temperature 1 and in the greedy limit, each as a
+    CUDA graph; per call: time, logits bytes / time against the measured HBM
+    peak, and the acceptance the samples give."""
+    lg, u = synth.sampling_inputs(wl_idx, depth, n_nodes, inp.draft_tok)
+    logits = torch.from_numpy(lg).to(dev)
+    u01 = torch.from_numpy(u).to(dev)
+    del lg
+    sample_tok = torch.empty(wl.B, wl.Qc, dtype=torch.int32, device=dev)
+    node_p = torch.empty(wl.B, wl.Qc, dtype=torch.float32, device=dev)
+    clean = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev).fill_(1.0)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    hbm_gbs, _, peak_src = load_peaks()
+    nbytes = logits.numel() * 4 + u01.numel() * 4 + sample_tok.numel() * 4 + node_p.numel() * 4
+    out = {"rows": wl.B * wl.Qc, "vocab": wl.vocab, "logits_bytes": logits.numel() * 4,
+           "algorithmic_bytes_per_call": nbytes}
+    for name, tau in (("temperature_1", 1.0), ("greedy", 0.0)):
+        with torch.cuda.stream(s):
+            ddtree.ddt_tree_sample(tree, logits, tau, u01, sample_tok, node_p, stream=s)
+        torch.cuda.synchronize()
+        gs = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gs, stream=s):
+            ddtree.ddt_tree_sample(tree, logits, tau, u01, sample_tok, node_p, stream=s)
+        evs = []
+        with torch.cuda.stream(s):
+            for it in range(n + 3):
+                flush.fill_(1)
+                torch.sum(clean, dim=0, out=sink)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                gs.replay()
+                e1.record(s)
+                evs.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs[3:])
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"us": ms * 1e3, "achieved_gbs": gbs, "peak_gbs": hbm_gbs, "frac": gbs / hbm_gbs}
+    # acceptance of the temperature-1 samples (the last timed calls were greedy)
+    with torch.cuda.stream(s):
+        ddtree.ddt_tree_sample(tree, logits, 1.0, u01, sample_tok, node_p, stream=s)
+        acc = ddtree.ddt_tree_accept(tree, sample_tok, stream=s)
+    torch.cuda.synchronize()
+    out["mean_accept_len_temperature_1"] = float(acc.accept_len.float().mean().item())
+    out["peak_source"] = f"{peak_src} HBM copy bandwidth"
+    out["bound"] = "hbm"
+    del logits, clean
+    return out
+
+
 def gpu_arm(args, wl_idx, rank, world, local_rank):
     import torch
 
@@ -446,6 +495,14 @@ def gpu_arm(args, wl_idx, rank, world, local_rank):
                  "note": "latency-bound: one block per sequence, at most 16 rows of 1152 B moved"}
     del kv_s, kr_s
 
+    # ---- temperature sampling at every tree node (the sampling commit path)
+    # on synthetic target logits [B,Qc,V] float32, then the accept walk on the
+    # samples; the kernel streams the logits once, so it is HBM-bound. Timed
+    # after writing the L2 flush buffer and then reading another buffer of
+    # that size, so the kernel starts on a cold L2 that holds no dirty lines.
+    sample = sample_leg(ddtree, wl_idx, wl, inp, depth, n_nodes, step.tree, s, flush, dev,
+                        max(args.steps, 10), torch)
+
     # ---- end to end through the public API with host buffers
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     h_tok, h_lp, h_root = pin(inp.draft_tok), pin(inp.draft_lp), pin(inp.root_tok)
@@ -512,6 +569,7 @@ def gpu_arm(args, wl_idx, rank, world, local_rank):
         "kv_commit": kv_commit,
         "paged_attn": paged,
         "bf16_out_attn": bf16_out,
+        "tree_sample": sample,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
