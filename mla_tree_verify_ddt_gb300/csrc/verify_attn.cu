@@ -888,32 +888,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // Merge per-chunk normalised partials: lse = log sum_c exp(lse_c),
-// out = sum_c exp(lse_c - lse) out_c. One 128-thread block per row.
+// out = sum_c exp(lse_c - lse) out_c. One 128-thread block per row; the
+// row's lse values are read in parallel into shared memory, then each thread
+// issues its float4 of every chunk before using any (the loads are in flight
+// together instead of one per chunk in turn).
 __global__ void __launch_bounds__(128)
     merge_chunks_kernel(size_t rows_total, int nsplit, const float *__restrict__ ws_o,
                         const float *__restrict__ ws_lse, void *__restrict__ out, int out_bf16,
                         float *__restrict__ lse) {
+    __shared__ float wsh[64];
+    __shared__ float stat[2];
     // the accept may start now; the partials are complete once the
     // attention grid is
     grid_dep_launch();
     grid_dep_wait();
     const size_t r = blockIdx.x;
     if (r >= rows_total) return;
-    float mx = -INFINITY;
-    for (int c = 0; c < nsplit; ++c) mx = fmaxf(mx, ws_lse[c * rows_total + r]);
+    const int t = threadIdx.x;
+    if (t < 32) {
+        // lse of chunks t and t + 32 (nsplit <= 64), their maximum, weights, sum
+        const float l0 = t < nsplit ? ws_lse[t * rows_total + r] : -INFINITY;
+        const float l1 = t + 32 < nsplit ? ws_lse[(t + 32) * rows_total + r] : -INFINITY;
+        float mx = fmaxf(l0, l1);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float w0 = (mx == -INFINITY || l0 == -INFINITY) ? 0.f : __expf(l0 - mx);
+        const float w1 = (mx == -INFINITY || l1 == -INFINITY) ? 0.f : __expf(l1 - mx);
+        float sum = w0 + w1;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        wsh[t] = w0;
+        wsh[t + 32] = w1;
+        if (t == 0) {
+            stat[0] = mx;
+            stat[1] = sum;
+        }
+    }
+    __syncthreads();
+    const float mx = stat[0], sum = stat[1];
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float sum = 0.f;
     if (mx != -INFINITY) {
-        for (int c = 0; c < nsplit; ++c) {
-            const float lc = ws_lse[c * rows_total + r];
-            if (lc == -INFINITY) continue;
-            const float w = __expf(lc - mx);
-            sum += w;
-            const float4 v = reinterpret_cast<const float4 *>(ws_o + (c * rows_total + r) * 512)[threadIdx.x];
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+        const float4 *src = reinterpret_cast<const float4 *>(ws_o) + r * 128 + t;
+        for (int c0 = 0; c0 < nsplit; c0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                v[u] = (c0 + u < nsplit && wsh[c0 + u] != 0.f) ? src[(c0 + u) * rows_total * 128]
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float w = c0 + u < nsplit ? wsh[c0 + u] : 0.f;
+                acc.x += w * v[u].x;
+                acc.y += w * v[u].y;
+                acc.z += w * v[u].z;
+                acc.w += w * v[u].w;
+            }
         }
         const float inv = 1.0f / sum;
         acc.x *= inv;
@@ -922,11 +951,11 @@ __global__ void __launch_bounds__(128)
         acc.w *= inv;
     }
     if (out_bf16)
-        reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + r * 512)[threadIdx.x] =
+        reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + r * 512)[t] =
             make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
     else
-        reinterpret_cast<float4 *>(static_cast<float *>(out) + r * 512)[threadIdx.x] = acc;
-    if (threadIdx.x == 0) lse[r] = (mx == -INFINITY) ? -INFINITY : mx + __logf(sum);
+        reinterpret_cast<float4 *>(static_cast<float *>(out) + r * 512)[t] = acc;
+    if (t == 0) lse[r] = (mx == -INFINITY) ? -INFINITY : mx + __logf(sum);
 }
 
 // ---------------------------------------------------------------- host side
