@@ -862,10 +862,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!seq_ok && mt == 0 && rank == 0 && chunk == 0 && !*abort_flag) a.status[b] = DDT_E_BADINPUT;
     }
     tc_fence_before();
-    // every softmax warp has staged its part of the output block: one thread
-    // stores the CTA's 128 x 256 block; the tensor map has the sequence's rows
-    // as one dimension, so rows past the sequence are not written
-    __syncthreads();
+    // Neither CTA may leave while its partner can still write into it. The
+    // output block and the lse are stored after this barrier, so its release
+    // arrivals do not wait for them (measured: a tensor store issued before
+    // it held the barrier about 2.5 us).
+    cluster_sync();
+    // every softmax warp has staged its part of the output block (the
+    // barrier above orders that for the whole CTA): one thread stores the
+    // CTA's 128 x 256 block; the tensor map has the sequence's rows as one
+    // dimension, so rows past the sequence are not written
     const bool store_out = tid == 0 && nrange > 0 && !*abort_flag;
     if (store_out) {
         // eight float32 boxes of 32 columns, or four bfloat16 boxes of 64
@@ -875,10 +880,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                          b + a.B * chunk);
         bulk_commit_group();
     }
-    // Neither CTA may leave while its partner can still write into it. The
-    // lse stores come after this barrier so its release arrivals do not wait
-    // for them.
-    cluster_sync();
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
