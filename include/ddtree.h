@@ -249,7 +249,7 @@ int ddt_kv_commit(const ddt_accept *acc, int B, int D, int Tcap, void *c_kv, voi
  * whose largest logit is +-inf, gets sample -1, children's node_p 0 and
  * DDT_E_BADINPUT in tree->status[b]; so does a child token outside
  * [0, vocab). Host errors: DDT_E_INVAL for a null pointer, vocab < 4 or not
- * a multiple of 4 or above 393216 (196608 on a device without 16-CTA
+ * a multiple of 4 or above 2883584 (1441792 on a device without 16-CTA
  * clusters), misaligned logits, a NaN or infinite temperature, a positive
  * temperature below 1e-30, or tree shape out of range. Reads tree->token,
  * tree->parent, tree->n_nodes; allocates nothing. */

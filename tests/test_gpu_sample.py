@@ -215,3 +215,28 @@ def test_repeated_calls_are_bitwise_identical():
     b = run_gpu(ot, wl.D, lg, 1.0, u)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1].view(np.uint32), b[1].view(np.uint32))
+
+
+def test_many_rows_take_several_launches():
+    """2500 sequences x 65 slots with random node counts over a 4-token
+    vocabulary: more rows than one launch gives its clusters (128 each), and
+    many padding slots in the row lists."""
+    rng = np.random.default_rng(21)
+    B, Qc, V = 2500, 65, 4
+    n = rng.integers(1, Qc + 1, B).astype(np.int32)
+    ot = star_oracle_tree(B, Qc, rng.integers(0, V, (B, Qc)), n)
+    lg = rng.standard_normal((B, Qc, V)).astype(np.float32)
+    u = rng.random((B, Qc), dtype=np.float32)
+    for tau in (0.0, 0.8):
+        g = run_gpu(ot, 1, lg, tau, u)
+        want = check(ot, lg, tau, u, *g[:3])
+        assert (g[0][want < 0] == -1).all() and (want < 0).sum() > 0
+
+
+def test_vocabulary_past_the_limit_is_rejected():
+    ot = star_oracle_tree(1, 2)
+    t = dev_tree(ot, 1)
+    big = torch.empty(2, 2883588, dtype=torch.float32, device="cuda")  # never read
+    with pytest.raises(ddtree.DdtError) as e:
+        ddtree.ddt_tree_sample(t, big.view(1, 2, -1), 1.0, torch.zeros(1, 2, device="cuda"))
+    assert e.value.code == ddtree.DDT_E_INVAL
