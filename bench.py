@@ -503,40 +503,60 @@ def gpu_arm(args, wl_idx, rank, world, local_rank):
     sample = sample_leg(ddtree, wl_idx, wl, inp, depth, n_nodes, step.tree, s, flush, dev,
                         max(args.steps, 10), torch)
 
-    # ---- end to end through the public API with host buffers
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    h_tok, h_lp, h_root = pin(inp.draft_tok), pin(inp.draft_lp), pin(inp.root_tok)
-    h_ql = pin(inp.q_lat.view(np.int16))
-    h_qr = pin(inp.q_rope.view(np.int16))
-    h_tg = pin(tg.cpu().numpy())
-    h_pl = pin(inp.prefix_len)
+    # ---- end to end through the public API with host buffers: the step's
+    # inputs sit in one pinned host buffer laid out like one device buffer
+    # whose views are the step's input tensors (one copy in), the node KV rows
+    # go one copy per sequence and tensor, and the accept result comes back in
+    # one copy (its four arrays are views of one device buffer)
+    D1 = wl.D + 1
+    fields = [("tok", (wl.B, wl.D, wl.K), torch.int32, inp.draft_tok), ("lp", (wl.B, wl.D, wl.K), torch.float32,
+              inp.draft_lp), ("root", (wl.B,), torch.int32, inp.root_tok),
+              ("ql", (wl.B, wl.Qc, wl.H, 512), torch.int16, inp.q_lat.view(np.int16)),
+              ("qr", (wl.B, wl.Qc, wl.H, 64), torch.int16, inp.q_rope.view(np.int16)),
+              ("tg", (wl.B, wl.Qc), torch.int32, tg.cpu().numpy()), ("pl", (wl.B,), torch.int32, inp.prefix_len)]
+
+    def packed(specs, device, pin):
+        offs, off = [], 0
+        for _, shape, dt, _ in specs:
+            offs.append(off)
+            off += (int(np.prod(shape)) * torch.empty((), dtype=dt).element_size() + 255) // 256 * 256
+        buf = torch.empty(off, dtype=torch.uint8, device=device)
+        if pin:
+            buf = buf.pin_memory()
+        views = {}
+        for (name, shape, dt, _), o in zip(specs, offs):
+            n = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+            views[name] = buf[o:o + n].view(dt).view(shape)
+        return buf, views
+
+    h_in, hv = packed(fields, "cpu", True)
+    d_in, dv = packed(fields, dev, False)
+    for name, _, _, arr in fields:
+        hv[name].copy_(torch.from_numpy(np.ascontiguousarray(arr)))
+    out_fields = [("accept_len", (wl.B,), torch.int32, None), ("accept_idx", (wl.B, D1), torch.int32, None),
+                  ("commit_tok", (wl.B, D1), torch.int32, None), ("next_root", (wl.B,), torch.int32, None)]
+    d_out, ov = packed(out_fields, dev, False)
+    h_out = torch.empty(d_out.numel(), dtype=torch.uint8).pin_memory()
+    step_e = ddtree.VerifyStep(dv["tok"], dv["lp"], dv["root"], wl.vocab, wl.budget, dv["ql"].view(torch.bfloat16),
+                               dv["qr"].view(torch.bfloat16), c_kv, k_rope, dv["pl"], dv["tg"], inp.scale,
+                               acc=ddtree.Accept(ov["accept_len"], ov["accept_idx"], ov["commit_tok"],
+                                                 ov["next_root"]))
     node_rows = [(b, int(inp.prefix_len[b])) for b in range(wl.B)]
-    h_ckv_nodes = [pin(inp.c_kv[b, T:T + wl.Qc].view(np.int16)) for b, T in node_rows]
-    h_kr_nodes = [pin(inp.k_rope[b, T:T + wl.Qc].view(np.int16)) for b, T in node_rows]
-    o_len = torch.empty(wl.B, dtype=torch.int32).pin_memory()
-    o_tok = torch.empty(wl.B, wl.D + 1, dtype=torch.int32).pin_memory()
-    o_root = torch.empty(wl.B, dtype=torch.int32).pin_memory()
-    ql16, qr16 = q_lat.view(torch.int16), q_rope.view(torch.int16)
+    h_ckv_nodes = [torch.from_numpy(np.ascontiguousarray(inp.c_kv[b, T:T + wl.Qc].view(np.int16))).pin_memory()
+                   for b, T in node_rows]
+    h_kr_nodes = [torch.from_numpy(np.ascontiguousarray(inp.k_rope[b, T:T + wl.Qc].view(np.int16))).pin_memory()
+                  for b, T in node_rows]
     ckv16, kr16 = c_kv.view(torch.int16), k_rope.view(torch.int16)
-    h2d = sum(t.numel() * t.element_size() for t in
-              [h_tok, h_lp, h_root, h_ql, h_qr, h_tg, h_pl, *h_ckv_nodes, *h_kr_nodes])
-    d2h = sum(t.numel() * t.element_size() for t in (o_len, o_tok, o_root))
+    h2d = h_in.numel() + sum(t.numel() * t.element_size() for t in [*h_ckv_nodes, *h_kr_nodes])
+    d2h = h_out.numel()
 
     def e2e_step():
-        tok.copy_(h_tok, non_blocking=True)
-        lp.copy_(h_lp, non_blocking=True)
-        root.copy_(h_root, non_blocking=True)
-        ql16.copy_(h_ql, non_blocking=True)
-        qr16.copy_(h_qr, non_blocking=True)
-        tg.copy_(h_tg, non_blocking=True)
-        pl.copy_(h_pl, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         for (b, T), hc, hk in zip(node_rows, h_ckv_nodes, h_kr_nodes):
             ckv16[b, T:T + wl.Qc].copy_(hc, non_blocking=True)
             kr16[b, T:T + wl.Qc].copy_(hk, non_blocking=True)
-        step.run(s)
-        o_len.copy_(step.acc.accept_len, non_blocking=True)
-        o_tok.copy_(step.acc.commit_tok, non_blocking=True)
-        o_root.copy_(step.acc.next_root, non_blocking=True)
+        step_e.run(s)
+        h_out.copy_(d_out, non_blocking=True)
 
     with torch.cuda.stream(s):
         for _ in range(args.warmup):
@@ -553,6 +573,8 @@ def gpu_arm(args, wl_idx, rank, world, local_rank):
             e1.synchronize()  # the host needs the accept result before the next step
             e2e_ms.append(e0.elapsed_time(e1))
     e2e_value = world * 1000.0 / statistics.mean(e2e_ms)
+    # the result that came back is the device's
+    assert np.array_equal(h_out[:wl.B * 4].view(torch.int32).numpy(), step_e.acc.accept_len.cpu().numpy())
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -347,14 +347,14 @@ class VerifyStep:
     """
 
     def __init__(self, tok, lp, root_tok, vocab: int, budget: int, q_lat, q_rope, c_kv, k_rope,
-                 prefix_len, target_argmax, scale: float):
+                 prefix_len, target_argmax, scale: float, acc: "Accept | None" = None):
         _contig(tok, lp, root_tok, q_lat, q_rope, c_kv, k_rope, prefix_len, target_argmax)
         dev = tok.device
         B, D, K = tok.shape
         H = q_lat.shape[2]
         self.inputs = (tok, lp, root_tok, q_lat, q_rope, c_kv, k_rope, prefix_len, target_argmax)
         self.tree = Tree.empty(B, D, budget, dev)
-        self.acc = Accept.empty(B, D, dev)
+        self.acc = acc if acc is not None else Accept.empty(B, D, dev)
         self.out = torch.empty(B, budget + 1, H, LATENT, dtype=torch.float32, device=dev)
         self.lse = torch.empty(B, budget + 1, H, dtype=torch.float32, device=dev)
         self.ws_bytes = ddt_workspace_size(B, D, K, budget, H, c_kv.shape[1])
