@@ -889,10 +889,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // Merge per-chunk normalised partials: lse = log sum_c exp(lse_c),
-// out = sum_c exp(lse_c - lse) out_c. One 128-thread block per row; the
-// row's lse values are read in parallel into shared memory, then each thread
-// issues its float4 of every chunk before using any (the loads are in flight
-// together instead of one per chunk in turn).
+// out = sum_c exp(lse_c - lse) out_c. One 128-thread block per row; each
+// thread owns one float4 of the row. The float4 of the first kAhead chunks
+// are loaded before the weights are known, together with the row's lse
+// values, so one memory round trip serves both; a chunk of weight 0 (no
+// visible key) contributes nothing, whatever its partial holds. Chunks past
+// kAhead are read in batches of 8 once the weights are known. kAhead (4, 8
+// or 16) follows the chunk count: registers held for loads that are never
+// issued would only lower the occupancy.
+template <int kAhead>
 __global__ void __launch_bounds__(128)
     merge_chunks_kernel(size_t rows_total, int nsplit, const float *__restrict__ ws_o,
                         const float *__restrict__ ws_lse, void *__restrict__ out, int out_bf16,
@@ -906,6 +911,11 @@ __global__ void __launch_bounds__(128)
     const size_t r = blockIdx.x;
     if (r >= rows_total) return;
     const int t = threadIdx.x;
+    const float4 *src = reinterpret_cast<const float4 *>(ws_o) + r * 128 + t;
+    float4 ahead[kAhead];
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u)
+        ahead[u] = u < nsplit ? src[u * rows_total * 128] : make_float4(0.f, 0.f, 0.f, 0.f);
     if (t < 32) {
         // lse of chunks t and t + 32 (nsplit <= 64), their maximum, weights, sum
         const float l0 = t < nsplit ? ws_lse[t * rows_total + r] : -INFINITY;
@@ -928,22 +938,27 @@ __global__ void __launch_bounds__(128)
     __syncthreads();
     const float mx = stat[0], sum = stat[1];
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](float w, const float4 &v) {
+        if (w != 0.f) {
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
+    };
     if (mx != -INFINITY) {
-        const float4 *src = reinterpret_cast<const float4 *>(ws_o) + r * 128 + t;
-        for (int c0 = 0; c0 < nsplit; c0 += 8) {
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u)
+            if (u < nsplit) add(wsh[u], ahead[u]);
+        for (int c0 = kAhead; c0 < nsplit; c0 += 8) {
             float4 v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u)
                 v[u] = (c0 + u < nsplit && wsh[c0 + u] != 0.f) ? src[(c0 + u) * rows_total * 128]
                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float w = c0 + u < nsplit ? wsh[c0 + u] : 0.f;
-                acc.x += w * v[u].x;
-                acc.y += w * v[u].y;
-                acc.z += w * v[u].z;
-                acc.w += w * v[u].w;
-            }
+            for (int u = 0; u < 8; ++u)
+                if (c0 + u < nsplit) add(wsh[c0 + u], v[u]);
         }
         const float inv = 1.0f / sum;
         acc.x *= inv;
@@ -1105,7 +1120,9 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
                       a) != cudaSuccess)
         return DDT_E_CUDA;
     if (plan.nsplit > 1) {
-        if (launch_kernel(merge_chunks_kernel, dim3(static_cast<unsigned>(rows_total)), dim3(128), 0, s, after_prev,
+        auto merge = plan.nsplit <= 4 ? merge_chunks_kernel<4>
+                     : plan.nsplit <= 8 ? merge_chunks_kernel<8> : merge_chunks_kernel<16>;
+        if (launch_kernel(merge, dim3(static_cast<unsigned>(rows_total)), dim3(128), 0, s, after_prev,
                           static_cast<size_t>(rows_total), plan.nsplit, static_cast<const float *>(ws_o),
                           static_cast<const float *>(ws_lse), static_cast<void *>(out.out), out_bf16 ? 1 : 0,
                           out.lse) != cudaSuccess)
