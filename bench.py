@@ -338,7 +338,9 @@ def gpu_arm(args, wl_idx, rank, world, local_rank):
     step = ddtree.VerifyStep(tok, lp, root, wl.vocab, wl.budget, q_lat, q_rope, c_kv, k_rope, pl,
                              tg, inp.scale)
     plan_nsplit = step.ws_bytes and (step.ws_bytes // (wl.B * wl.Qc * wl.H * 513 * 4)) or 1
-    launches_per_step = 3 + (1 if plan_nsplit > 1 else 0)
+    # tree build, attention, and the merge that also runs the accept (or the
+    # accept alone when the key range is not split)
+    launches_per_step = 3
 
     s = torch.cuda.Stream(device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)

@@ -162,8 +162,12 @@ int ddt_verify_mla_attn(const ddt_attn_in *in, const ddt_tree *tree, float scale
 int ddt_tree_accept(const ddt_tree *tree, const int32_t *target_argmax, ddt_accept *out,
                     void *stream);
 
-/* Steps 1-3 enqueued back to back on one stream (build, attention, key-range
- * merge when the key range is split, accept) with no host synchronisation. */
+/* Steps 1-3 enqueued back to back on one stream with no host
+ * synchronisation: three launches. The tree build; the attention; then,
+ * when the key range is split, the key-range merge, whose grid also runs the
+ * accept walk (one warp per sequence, in blocks of its own), else the accept
+ * alone. Results are identical to ddt_tree_build + ddt_verify_mla_attn +
+ * ddt_tree_accept on the same stream. */
 int ddt_verify_step(const ddt_draft *draft, int budget, ddt_tree *tree,
                     const ddt_attn_in *attn, float scale, ddt_attn_out *attn_out,
                     const int32_t *target_argmax, ddt_accept *acc, void *workspace,

@@ -177,10 +177,15 @@ int ddt_verify_step(const ddt_draft *draft, int budget, ddt_tree *tree, const dd
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (ddt::launch_tree_build(*draft, budget, *tree, s) != cudaSuccess) return DDT_E_CUDA;
     // the attention starts while the tree is being built (it waits, in the
-    // kernel, before it reads the tree); the accept runs beside the merge
-    if (int rc = ddt::launch_verify_attn(*attn, *tree, scale, *attn_out, workspace, ws_bytes, plan, s, true))
+    // kernel, before it reads the tree); with split keys the merge kernel
+    // also runs the accept walk, else the accept follows the attention
+    const ddt::AcceptArgs acc_args = ddt::accept_args(*tree, target_argmax, *acc);
+    bool accepted = false;
+    if (int rc = ddt::launch_verify_attn(*attn, *tree, scale, *attn_out, workspace, ws_bytes, plan, s, true,
+                                         nullptr, 0, false, &acc_args, &accepted))
         return rc;
-    if (ddt::launch_tree_accept(*tree, target_argmax, *acc, s, true) != cudaSuccess) return DDT_E_CUDA;
+    if (!accepted && ddt::launch_tree_accept(*tree, target_argmax, *acc, s, true) != cudaSuccess)
+        return DDT_E_CUDA;
     return DDT_OK;
 }
 

@@ -21,6 +21,14 @@ cudaError_t launch_tree_build(const ddt_draft &in, int budget, const ddt_tree &o
 cudaError_t launch_tree_accept(const ddt_tree &tree, const int32_t *target,
                                const ddt_accept &out, cudaStream_t s, bool after_prev = false);
 
+// The greedy accept walk's inputs and outputs (accept_walk.cuh).
+struct AcceptArgs {
+    int B, D, Qc;
+    const int32_t *token, *parent, *n_nodes, *target;
+    int32_t *accept_len, *accept_idx, *commit_tok, *next_root;
+};
+AcceptArgs accept_args(const ddt_tree &tree, const int32_t *target, const ddt_accept &out);
+
 struct AttnPlan {
     int mtiles;       // 128-row tiles of Qc*H rows per sequence
     int nsplit;       // key-range chunks per (sequence, row tile)
@@ -31,11 +39,14 @@ struct AttnPlan {
 AttnPlan plan_attention(int B, int Qc, int H, int Tcap, int sms);
 
 // Encodes the tensor maps and enqueues the attention kernel (and the merge
-// kernel when nsplit > 1).
+// kernel when nsplit > 1). With `fused_accept`, a merge kernel also runs the
+// accept walk in extra blocks of its grid and sets *accepted; without a
+// merge nothing is fused and *accepted stays false.
 int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
                        const ddt_attn_out &out, void *workspace, size_t ws_bytes,
                        const AttnPlan &plan, cudaStream_t s, bool after_prev = false,
-                       const int32_t *kv_index = nullptr, int pool_rows = 0, bool out_bf16 = false);
+                       const int32_t *kv_index = nullptr, int pool_rows = 0, bool out_bf16 = false,
+                       const AcceptArgs *fused_accept = nullptr, bool *accepted = nullptr);
 
 // cudaLaunchKernelEx with the programmatic-stream-serialization attribute
 // when `after_prev`, a plain launch otherwise.

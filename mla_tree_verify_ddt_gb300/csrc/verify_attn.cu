@@ -59,6 +59,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "accept_walk.cuh"
 #include "ddt_internal.h"
 #include "ddt_ptx.cuh"
 
@@ -897,20 +898,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // kAhead are read in batches of 8 once the weights are known. kAhead (4, 8
 // or 16) follows the chunk count: registers held for loads that are never
 // issued would only lower the occupancy.
+// Inside a verify step the grid has ceil(B / 4) blocks more, whose warps run
+// the accept walk of one sequence each (it needs only the tree, complete
+// before the attention kernel let this grid start), so the step needs no
+// launch of its own for the accept.
+// The partials are read through plain pointers, not const __restrict__ ones:
+// this grid starts while the attention grid still writes them, so they are
+// not read-only for its lifetime, and a restrict-qualified load may be
+// hoisted above the dependency wait or served by the non-coherent cache.
 template <int kAhead>
 __global__ void __launch_bounds__(128)
-    merge_chunks_kernel(size_t rows_total, int nsplit, const float *__restrict__ ws_o,
-                        const float *__restrict__ ws_lse, void *__restrict__ out, int out_bf16,
-                        float *__restrict__ lse) {
+    merge_chunks_kernel(size_t rows_total, int nsplit, const float *ws_o, const float *ws_lse,
+                        void *__restrict__ out, int out_bf16, float *__restrict__ lse, const AcceptArgs walk) {
     __shared__ float wsh[64];
     __shared__ float stat[2];
-    // the accept may start now; the partials are complete once the
-    // attention grid is
+    // work later on the stream may start now; the partials are complete once
+    // the attention grid is
     grid_dep_launch();
-    grid_dep_wait();
     const size_t r = blockIdx.x;
-    if (r >= rows_total) return;
     const int t = threadIdx.x;
+    if (r >= rows_total) {
+        const int b = static_cast<int>(r - rows_total) * 4 + (t >> 5);
+        if (b < walk.B) accept_walk(walk, b, t & 31);
+        return;
+    }
+    grid_dep_wait();
     const float4 *src = reinterpret_cast<const float4 *>(ws_o) + r * 128 + t;
     float4 ahead[kAhead];
 #pragma unroll
@@ -1057,7 +1069,8 @@ AttnPlan plan_attention(int B, int Qc, int H, int Tcap, int sms) {
 int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
                        const ddt_attn_out &out, void *workspace, size_t ws_bytes,
                        const AttnPlan &plan, cudaStream_t s, bool after_prev, const int32_t *kv_index,
-                       int pool_rows, bool out_bf16) {
+                       int pool_rows, bool out_bf16, const AcceptArgs *fused_accept, bool *accepted) {
+    if (accepted) *accepted = false;
     EncodeTiledFn enc = get_encoder();
     if (!enc) return DDT_E_CUDA;
     const uint64_t rows_total = static_cast<uint64_t>(tree.B) * tree.Qc * in.H;
@@ -1122,11 +1135,15 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
     if (plan.nsplit > 1) {
         auto merge = plan.nsplit <= 4 ? merge_chunks_kernel<4>
                      : plan.nsplit <= 8 ? merge_chunks_kernel<8> : merge_chunks_kernel<16>;
-        if (launch_kernel(merge, dim3(static_cast<unsigned>(rows_total)), dim3(128), 0, s, after_prev,
+        AcceptArgs acc{};  // B = 0: no accept blocks
+        if (fused_accept) acc = *fused_accept;
+        const uint64_t blocks = rows_total + (static_cast<uint64_t>(acc.B) + 3) / 4;
+        if (launch_kernel(merge, dim3(static_cast<unsigned>(blocks)), dim3(128), 0, s, after_prev,
                           static_cast<size_t>(rows_total), plan.nsplit, static_cast<const float *>(ws_o),
                           static_cast<const float *>(ws_lse), static_cast<void *>(out.out), out_bf16 ? 1 : 0,
-                          out.lse) != cudaSuccess)
+                          out.lse, acc) != cudaSuccess)
             return DDT_E_CUDA;
+        if (accepted && fused_accept) *accepted = true;
     }
     return DDT_OK;
 }

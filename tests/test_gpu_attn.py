@@ -93,6 +93,21 @@ def test_full_parity_custom(seed, B, D, K, budget, H, T, underfull):
     full_check(inp, f"custom seed {seed}")
 
 
+@pytest.mark.parametrize("seed,T,lo,hi", [
+    (7, 1500, 5, 8),     # the merge's 8-wide early loads
+    (8, 6000, 17, 64),   # 16 early loads, then the rest in batches of 8
+])
+def test_full_parity_many_key_range_chunks(seed, T, lo, hi):
+    """One row tile (9 nodes x 4 heads) over a long prefix: the keys split
+    into many ranges, so the merge's wider variants and its batch loop run."""
+    inp = custom_inputs(seed, 1, 4, 4, 8, 4, [T])
+    wl = inp.wl
+    ws = ddtree.ddt_workspace_size(1, wl.D, wl.K, wl.budget, wl.H, inp.Tcap)
+    nsplit = ws // (wl.Qc * wl.H * 513 * 4)
+    assert lo <= nsplit <= hi, f"{nsplit} key-range chunks"
+    full_check(inp, f"{nsplit} key-range chunks")
+
+
 @pytest.mark.parametrize("idx", [2, 3, 4])
 def test_sampled_parity_large_workloads(idx):
     inp = synth.make_inputs(idx)
