@@ -150,9 +150,11 @@ int ddt_tree_build(const ddt_draft *in, int budget, ddt_tree *out, void *stream)
  * over the visible rows j: 0..T_b-1 and T_b+m for every bit m set in
  * mask[b,i]; out = sum_j softmax(s)_j * c_kv[b,j]; lse = log sum_j exp(s_j).
  * Computed with bfloat16 tensor-core products, float32 accumulation and a
- * float32 online softmax. `workspace` must hold ddt_workspace_size(...)
- * bytes (it may be NULL when that is 0). Reads tree->mask, tree->n_nodes and
- * writes DDT_E_BADINPUT / DDT_E_TIMEOUT into tree->status. */
+ * float32 online softmax. `scale` must be positive and finite (else
+ * DDT_E_INVAL; 1/sqrt(192) for the absorbed 128+64 head dimension).
+ * `workspace` must hold ddt_workspace_size(...) bytes (it may be NULL when
+ * that is 0). Reads tree->mask, tree->n_nodes and writes DDT_E_BADINPUT /
+ * DDT_E_TIMEOUT into tree->status. */
 int ddt_verify_mla_attn(const ddt_attn_in *in, const ddt_tree *tree, float scale,
                         ddt_attn_out *out, void *workspace, size_t ws_bytes, void *stream);
 

@@ -3,6 +3,7 @@
 // the device except ddt_read_device_status.
 #include <cuda_runtime.h>
 
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 
@@ -99,6 +100,10 @@ int check_accept(const ddt_tree *tree, const int32_t *target, const ddt_accept *
     return DDT_OK;
 }
 
+// The attention's score scale: positive and finite (the kernel applies it
+// after taking the maximum of the raw scores, which needs scale > 0).
+int check_scale(float scale) { return (scale > 0.f && scale <= FLT_MAX) ? DDT_OK : DDT_E_INVAL; }
+
 }  // namespace
 
 extern "C" {
@@ -123,6 +128,7 @@ int ddt_tree_build(const ddt_draft *in, int budget, ddt_tree *out, void *stream)
 int ddt_verify_mla_attn(const ddt_attn_in *in, const ddt_tree *tree, float scale, ddt_attn_out *out,
                         void *workspace, size_t ws_bytes, void *stream) {
     if (int rc = check_attn(in, tree, out)) return rc;
+    if (int rc = check_scale(scale)) return rc;
     if (int rc = check_device()) return rc;
     const ddt::AttnPlan plan = ddt::plan_attention(tree->B, tree->Qc, in->H, in->Tcap, device_info()->sms);
     if (plan.ws_bytes > ws_bytes || (plan.ws_bytes && !workspace)) return DDT_E_INVAL;
@@ -136,6 +142,7 @@ int ddt_verify_mla_attn_bf16(const ddt_attn_in *in, const ddt_tree *tree, float 
     // its pointer and alignment)
     ddt_attn_out out{reinterpret_cast<float *>(out_bf16), lse};
     if (int rc = check_attn(in, tree, &out)) return rc;
+    if (int rc = check_scale(scale)) return rc;
     if (int rc = check_device()) return rc;
     const ddt::AttnPlan plan = ddt::plan_attention(tree->B, tree->Qc, in->H, in->Tcap, device_info()->sms);
     if (plan.ws_bytes > ws_bytes || (plan.ws_bytes && !workspace)) return DDT_E_INVAL;
@@ -148,6 +155,7 @@ int ddt_verify_mla_attn_paged(const ddt_attn_in *in, const ddt_tree *tree, float
                               void *stream) {
     if (!kv_index || pool_rows < 1) return DDT_E_INVAL;
     if (int rc = check_attn(in, tree, out)) return rc;
+    if (int rc = check_scale(scale)) return rc;
     if (int rc = check_device()) return rc;
     const ddt::AttnPlan plan = ddt::plan_attention(tree->B, tree->Qc, in->H, in->Tcap, device_info()->sms);
     if (plan.ws_bytes > ws_bytes || (plan.ws_bytes && !workspace)) return DDT_E_INVAL;
@@ -170,6 +178,7 @@ int ddt_verify_step(const ddt_draft *draft, int budget, ddt_tree *tree, const dd
     // every check first, so an error enqueues nothing
     if (int rc = check_draft(draft, tree, budget)) return rc;
     if (int rc = check_attn(attn, tree, attn_out)) return rc;
+    if (int rc = check_scale(scale)) return rc;
     if (int rc = check_accept(tree, target_argmax, acc)) return rc;
     if (int rc = check_device()) return rc;
     const ddt::AttnPlan plan = ddt::plan_attention(tree->B, tree->Qc, attn->H, attn->Tcap, device_info()->sms);

@@ -745,13 +745,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t vis = ~0u;
             if (!node_ok) vis = 0;
             else if (key0 + 32 > T) vis = half_tile_visibility(key0, T, n, m0, m1);
+            // The scores stay unscaled: the scale (positive, checked on the
+            // host) is applied to their maximum here and folded into the
+            // exponent's FFMA below. Hidden keys become -inf, only in tiles
+            // where some lane has one.
             float mx = -INFINITY;
+            if (__all_sync(0xffffffffu, vis == ~0u)) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                if ((k & 7) == 0) ship_group(k >> 3);
-                s[k] = ((vis >> k) & 1u) ? s[k] * a.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[k]);
+                for (int k = 0; k < 32; ++k) {
+                    if ((k & 7) == 0) ship_group(k >> 3);
+                    mx = fmaxf(mx, s[k]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    if ((k & 7) == 0) ship_group(k >> 3);
+                    s[k] = ((vis >> k) & 1u) ? s[k] : -INFINITY;
+                    mx = fmaxf(mx, s[k]);
+                }
             }
+            mx *= a.scale_log2;
             float mx_other;
             if (!swap_with_other_half(jj, mx, mx_other)) {
                 ok = false;
@@ -766,13 +779,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             // P = hi + lo, both bf16. While no key has been visible yet
             // m_ref is -inf and every s is -inf: subtracting 0 keeps p = 0.
-            const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
+            const float nmref = (m_ref == -INFINITY) ? 0.f : -m_ref;
             uint32_t pw[32];  // 16 hi words, then 16 lo words
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 if ((k & 3) == 0) ship_group(4 + (k >> 2));
-                const float p0 = ex2_approx(s[2 * k] - mref);
-                const float p1 = ex2_approx(s[2 * k + 1] - mref);
+                const float p0 = ex2_approx(fmaf(s[2 * k], a.scale_log2, nmref));
+                const float p1 = ex2_approx(fmaf(s[2 * k + 1], a.scale_log2, nmref));
                 const uint32_t h = pack_bf16x2(p0, p1);
                 pw[k] = h;
                 pw[16 + k] = pack_bf16x2(p0 - bf16lo_to_f32(h), p1 - bf16hi_to_f32(h));

@@ -96,6 +96,20 @@ def test_attention_rejects_misaligned_and_null(L):
                                      ctypes.byref(o), None, 0, None) == ddtree.DDT_E_INVAL
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.07, float("nan"), float("inf")])
+def test_attention_rejects_scale_that_is_not_positive_and_finite(L, scale):
+    t = _tree()
+    a = ddtree.DdtAttnIn(4, 100, FAKE, FAKE, FAKE, FAKE, FAKE)
+    o = ddtree.DdtAttnOut(FAKE, FAKE)
+    sc = ctypes.c_float(scale)
+    assert L.ddt_verify_mla_attn(ctypes.byref(a), ctypes.byref(t), sc, ctypes.byref(o), None, 0,
+                                 None) == ddtree.DDT_E_INVAL
+    assert L.ddt_verify_mla_attn_bf16(ctypes.byref(a), ctypes.byref(t), sc, FAKE, FAKE, None, 0,
+                                      None) == ddtree.DDT_E_INVAL
+    assert L.ddt_verify_mla_attn_paged(ctypes.byref(a), ctypes.byref(t), sc, ctypes.byref(o), None, 0,
+                                       FAKE, 8, None) == ddtree.DDT_E_INVAL
+
+
 def test_accept_rejects_null(L):
     t = _tree()
     acc = ddtree.DdtAccept(FAKE, None, FAKE, FAKE)
