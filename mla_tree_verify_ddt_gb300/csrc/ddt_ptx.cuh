@@ -388,6 +388,39 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int ab_bf16, i
            | (static_cast<uint32_t>(M >> 4) << 24);       // M / 16
 }
 
+// max of three floats in one instruction (sm_100 and later); like fmaxf, a
+// NaN operand is ignored unless all three are NaN
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Packed float32 pairs (sm_100 and later): one instruction computes both
+// lanes, each rounded to nearest exactly as the scalar instruction would.
+__device__ __forceinline__ void add_f32x2(float a0, float a1, float b0, float b1, float &r0, float &r1) {
+    asm("{\n\t.reg .b64 a, b, r;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub_f32x2(float a0, float a1, float b0, float b1, float &r0, float &r1) {
+    asm("{\n\t.reg .b64 a, b, r;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// (a0, a1) * c + (d, d)
+__device__ __forceinline__ void fma_f32x2(float a0, float a1, float c, float d, float &r0, float &r1) {
+    asm("{\n\t.reg .b64 a, c, d, r;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 c, {%4, %4};\n\tmov.b64 d, {%5, %5};\n\t"
+        "fma.rn.f32x2 r, a, c, d;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(c), "f"(d));
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

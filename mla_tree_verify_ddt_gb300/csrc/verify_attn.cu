@@ -689,7 +689,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             make_uint4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]), r_bar_sx_full);
         };
 
-        float m_ref = -INFINITY, l_sum = 0.f;
+        // the row sum of this thread's keys, as the sums of its even and odd
+        // keys (one packed add per key pair)
+        float m_ref = -INFINITY, l_even = 0.f, l_odd = 0.f;
         bool ok = true;
         // The partial of tile t+1 is loaded and shipped before the softmax of
         // tile t, so its transfer to the partner overlaps that softmax.
@@ -709,15 +711,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
             }
             float s[32];
-            uint32_t read_dep = 0;  // depends on every word read from SX
+            // depends on every load from SX (a 128-bit load completes as a
+            // whole, so one word of each is enough)
+            uint32_t read_dep = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const uint4 o = sx[(grp0 + i) * kRows + row];
-                read_dep ^= o.x ^ o.y ^ o.z ^ o.w;
-                s[4 * i] = __uint_as_float(sv[4 * i]) + __uint_as_float(o.x);
-                s[4 * i + 1] = __uint_as_float(sv[4 * i + 1]) + __uint_as_float(o.y);
-                s[4 * i + 2] = __uint_as_float(sv[4 * i + 2]) + __uint_as_float(o.z);
-                s[4 * i + 3] = __uint_as_float(sv[4 * i + 3]) + __uint_as_float(o.w);
+                read_dep ^= o.x;
+                add_f32x2(__uint_as_float(sv[4 * i]), __uint_as_float(sv[4 * i + 1]), __uint_as_float(o.x),
+                          __uint_as_float(o.y), s[4 * i], s[4 * i + 1]);
+                add_f32x2(__uint_as_float(sv[4 * i + 2]), __uint_as_float(sv[4 * i + 3]), __uint_as_float(o.z),
+                          __uint_as_float(o.w), s[4 * i + 2], s[4 * i + 3]);
             }
             // hand the buffer back once every read of it is done (the arrive
             // waits for read_dep); a release would also wait for this
@@ -749,22 +753,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // host) is applied to their maximum here and folded into the
             // exponent's FFMA below. Hidden keys become -inf, only in tiles
             // where some lane has one.
-            float mx = -INFINITY;
-            if (__all_sync(0xffffffffu, vis == ~0u)) {
+            if (!__all_sync(0xffffffffu, vis == ~0u)) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    if ((k & 7) == 0) ship_group(k >> 3);
-                    mx = fmaxf(mx, s[k]);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    if ((k & 7) == 0) ship_group(k >> 3);
-                    s[k] = ((vis >> k) & 1u) ? s[k] : -INFINITY;
-                    mx = fmaxf(mx, s[k]);
-                }
+                for (int k = 0; k < 32; ++k) s[k] = ((vis >> k) & 1u) ? s[k] : -INFINITY;
             }
-            mx *= a.scale_log2;
+            // two three-input max chains over the 32 scores
+            float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 32; k += 4) {
+                if ((k & 7) == 0) ship_group(k >> 3);
+                mxa = fmax3(mxa, s[k], s[k + 1]);
+                mxb = fmax3(mxb, s[k + 2], s[k + 3]);
+            }
+            float mx = fmaxf(mxa, mxb) * a.scale_log2;
             float mx_other;
             if (!swap_with_other_half(jj, mx, mx_other)) {
                 ok = false;
@@ -775,7 +776,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (mx > m_ref + kRescaleThreshold) {
                 alpha = ex2_approx(m_ref - mx);  // 0 while nothing was visible before
                 m_ref = mx;
-                l_sum *= alpha;
+                l_even *= alpha;
+                l_odd *= alpha;
             }
             // P = hi + lo, both bf16. While no key has been visible yet
             // m_ref is -inf and every s is -inf: subtracting 0 keeps p = 0.
@@ -784,12 +786,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 if ((k & 3) == 0) ship_group(4 + (k >> 2));
-                const float p0 = ex2_approx(fmaf(s[2 * k], a.scale_log2, nmref));
-                const float p1 = ex2_approx(fmaf(s[2 * k + 1], a.scale_log2, nmref));
+                float e0, e1, r0, r1;
+                fma_f32x2(s[2 * k], s[2 * k + 1], a.scale_log2, nmref, e0, e1);
+                const float p0 = ex2_approx(e0);
+                const float p1 = ex2_approx(e1);
                 const uint32_t h = pack_bf16x2(p0, p1);
                 pw[k] = h;
-                pw[16 + k] = pack_bf16x2(p0 - bf16lo_to_f32(h), p1 - bf16hi_to_f32(h));
-                l_sum += p0 + p1;
+                sub_f32x2(p0, p1, bf16lo_to_f32(h), bf16hi_to_f32(h), r0, r1);
+                pw[16 + k] = pack_bf16x2(r0, r1);
+                add_f32x2(l_even, l_odd, p0, p1, l_even, l_odd);
             }
             // ---- rescale this thread's half of the row's O (needs PV of the
             // previous tile done), then publish P over the S it replaces
@@ -830,7 +835,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (ok && !resolved && !resolve_s()) ok = false;
         // the row sum is the two halves' sums (same reference max)
-        float l_other;
+        float l_sum = l_even + l_odd, l_other;
         if (ok && !swap_with_other_half(nrange, l_sum, l_other)) ok = false;
         if (ok) l_sum += l_other;
         if (ok && !wwait(bar(BAR_O_FINAL), 0)) ok = false;
