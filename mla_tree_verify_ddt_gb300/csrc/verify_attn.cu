@@ -83,11 +83,15 @@ constexpr int kOffQ = 0;
 constexpr int kOffRing = kOffQ + kQSmemChunks * kChunkBytesQ;     // 49152
 constexpr int kOffSX = kOffRing + kSlots * kSlotBytes;            // 196608: the partner's partial S of a tile
 constexpr int kSXBytes = kRows * kKeys * 4;                       // 32768
-constexpr int kOffBar = kOffSX + kSXBytes;                        // 229376: barriers and flags (256 B)
-constexpr int kOffTree = kOffBar + 256;                           // 229632: the tree as this CTA needs it
+constexpr int kOffBar = kOffSX + kSXBytes;                        // 229376: barriers and flags (272 B)
+constexpr int kOffTree = kOffBar + 272;                           // 229648: the tree as this CTA needs it
 constexpr int kMaxTileNodes = DDT_MAX_BUDGET + 1;                 // nodes a 128-row tile can span (<= Qc)
 constexpr int kTreeBytes = 16 + kMaxTileNodes * 16;               // node count, then 2 mask words per node
-constexpr int kSmemBytes = kOffTree + kTreeBytes + 1024;          // + alignment slack
+constexpr int kOffXRow = kOffTree + kTreeBytes;                   // 230704: one float per row, the two
+                                                                  // threads of a row combine through it
+constexpr int kSmemBytes = kOffXRow + kRows * 4 + 1024;           // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+static_assert(kOffXRow % 16 == 0, "row words aligned");
 constexpr int kOutBoxBytes = kRows * 128;                         // output staging: 128 rows x 32 fp32
 static_assert(8 * kOutBoxBytes <= kSlots * kSlotBytes, "output staging must fit in the KV ring");
 
@@ -97,7 +101,6 @@ constexpr uint32_t kColSP = 256;    // 3 x 64: partial S of a tile, overwritten 
                                     // lane, once read) by its P: 32 hi words then 32 lo words
 constexpr uint32_t kColQ3 = 448;    // 32: latent query chunk 3 (bf16 pairs)
 constexpr uint32_t kColQR = 480;    // 16: rotary query (bf16 pairs)
-constexpr uint32_t kColX = 496;     // 4: [round parity][key half] word the two threads of a row swap
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -119,11 +122,13 @@ enum {
     // exchange barriers, arrived on by the partner CTA's threads
     BAR_SX_FULL = 21,    // partner's partial S of the tile is in my SX
     BAR_SX_EMPTY = 22,   // partner has read the partial S I wrote into its SX
-    // the two threads of a row swap their halves' tile max (and, at the end,
-    // their row sums): one barrier per TMEM lane quadrant
-    BAR_MAXX = 23,       // 4
+    // the two threads of a row combine their halves' tile max (and, at the
+    // end, their row sums), per TMEM lane quadrant: XA the key-half-1 warp's
+    // value is in shared memory, XB the combined value is
+    BAR_XA = 23,         // 4
     BAR_TREE = 27,       // the tree's node count and this tile's node masks are in shared memory
-    NUM_BARS = 28
+    BAR_XB = 28,         // 4
+    NUM_BARS = 32        // (one per lane of the initialising warp)
 };
 
 // arrival count of barrier i (see the enum); with a block-table cache the
@@ -132,7 +137,6 @@ __device__ __forceinline__ uint32_t bar_count(int i, bool gathered) {
     if (gathered && i >= BAR_RING_FULL && i < BAR_RING_FULL + kSlots) return 64;  // two gather warps
     if (i == BAR_QT_READY || (i >= BAR_P_FULL && i < BAR_P_FULL + kSPBufs)) return 8;  // one per softmax warp
     if (i == BAR_SX_EMPTY) return 2 * kRows;  // every partner softmax thread
-    if (i >= BAR_MAXX && i < BAR_MAXX + 4) return 2;  // warps q and q+4
     return 1;  // one arrival (SX_FULL: the arming thread; its bytes come from the partner's st.async)
 }
 
@@ -644,20 +648,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto wwait_cluster = [&](uint32_t barrier, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait_cluster(barrier, parity, deadline, abort_flag));
         };
-        // The two threads of a row (same tensor-memory lane, warps q and
-        // q+4) swap one float through a tensor-memory word: round k uses the
-        // words of parity k&1 and phase k of the quadrant's barrier.
-        auto swap_with_other_half = [&](int k, float v, float &other) -> bool {
-            tmem_st1(tmem + lane_base + kColX + (k & 1) * 2 + half, __float_as_uint(v));
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_MAXX + quad));
-            if (!wwait(bar(BAR_MAXX + quad), k & 1)) return false;
-            __syncwarp();
-            tc_fence_after();
-            other = __uint_as_float(tmem_ld1(tmem + lane_base + kColX + (k & 1) * 2 + (half ^ 1)));
-            tmem_wait_ld();
+        // The two threads of a row (warps q and q+4) combine one float each
+        // round k through the row's shared-memory word: the key-half-1 thread
+        // writes its value, the key-half-0 thread reads it, combines (max or
+        // sum) and writes the result back, which the key-half-1 thread then
+        // reads; each hand-off is phase k of a barrier of the quadrant. The
+        // word is rewritten only after its last reader has arrived on the
+        // barrier the next writer waits for, so one word per row suffices.
+        float *xrow = reinterpret_cast<float *>(smem + kOffXRow) + row;
+        auto combine_halves = [&](int k, float v, bool sum, float &r) -> bool {
+            if (half == 1) {
+                *xrow = v;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_XA + quad));
+                if (!wwait(bar(BAR_XB + quad), k & 1)) return false;
+                r = *xrow;
+            } else {
+                if (!wwait(bar(BAR_XA + quad), k & 1)) return false;
+                const float o = *xrow;
+                r = sum ? v + o : fmaxf(v, o);
+                *xrow = r;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_XB + quad));
+            }
             return true;
         };
 
@@ -672,13 +685,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(BAR_QT_READY));
         }
 
-        // this CTA's partial S of tile t, this thread's 32 keys
-        auto load_own = [&](int t, uint32_t (&sv)[32]) -> bool {
-            const int sb = t % kSPBufs;
-            if (!wwait(bar(BAR_S_FULL + sb), (t / kSPBufs) & 1)) return false;
+        // this CTA's partial S of a tile (S/P buffer `buf`, barrier phase
+        // parity `par`), this thread's 32 keys
+        auto load_own = [&](int buf, uint32_t par, uint32_t (&sv)[32]) -> bool {
+            if (!wwait(bar(BAR_S_FULL + buf), par)) return false;
             __syncwarp();
             tc_fence_after();
-            tmem_ld32(tmem + lane_base + kColSP + sb * 64 + col_half, sv);
+            tmem_ld32(tmem + lane_base + kColSP + buf * 64 + col_half, sv);
             tmem_wait_ld();
             return true;
         };
@@ -696,13 +709,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // The partial of tile t+1 is loaded and shipped before the softmax of
         // tile t, so its transfer to the partner overlaps that softmax.
         uint32_t sv[32];
-        const bool ok0 = load_own(0, sv);
+        const bool ok0 = load_own(0, 0, sv);
         // the partner's barriers exist before this CTA's first remote operation
         cluster_wait();
         if (!ok0) ok = false;
         else ship(sv);
+        // tile jj's S/P buffer (jj % kSPBufs) and phase parity ((jj / kSPBufs) & 1),
+        // kept as running counters
+        int sb = 0;
+        uint32_t sph = 0;
         for (int jj = 0; jj < nrange && ok; ++jj) {
-            const int sb = jj % kSPBufs;
+            const int nb = sb == kSPBufs - 1 ? 0 : sb + 1;
+            const uint32_t nph = sb == kSPBufs - 1 ? sph ^ 1u : sph;
             const int key0 = (t0 + jj) * kKeys + half * 32;
             // ---- the partner's partial of tile jj: 128 rows x 256 B
             if (lead) mbar_arrive_expect_tx(bar(BAR_SX_FULL), kSXBytes);
@@ -732,7 +750,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // softmax below: the link to the partner drains at a few tens of
             // GB/s, and a burst of them would stall this thread until it has.
             const bool ship_next = jj + 1 < nrange;
-            if (ship_next && (!load_own(jj + 1, sv) || !wwait_cluster(bar(BAR_SX_EMPTY), jj & 1))) {
+            if (ship_next && (!load_own(nb, nph, sv) || !wwait_cluster(bar(BAR_SX_EMPTY), jj & 1))) {
                 ok = false;
                 break;
             }
@@ -766,12 +784,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mxb = fmax3(mxb, s[k + 2], s[k + 3]);
             }
             float mx = fmaxf(mxa, mxb) * a.scale_log2;
-            float mx_other;
-            if (!swap_with_other_half(jj, mx, mx_other)) {
+            if (!combine_halves(jj, mx, false, mx)) {
                 ok = false;
                 break;
             }
-            mx = fmaxf(mx, mx_other);
             float alpha = 1.0f;  // rescale factor of this row's O for this tile
             if (mx > m_ref + kRescaleThreshold) {
                 alpha = ex2_approx(m_ref - mx);  // 0 while nothing was visible before
@@ -832,12 +848,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(BAR_P_FULL + sb));
+            sb = nb;
+            sph = nph;
         }
         if (ok && !resolved && !resolve_s()) ok = false;
         // the row sum is the two halves' sums (same reference max)
-        float l_sum = l_even + l_odd, l_other;
-        if (ok && !swap_with_other_half(nrange, l_sum, l_other)) ok = false;
-        if (ok) l_sum += l_other;
+        float l_sum = l_even + l_odd;
+        if (ok && !combine_halves(nrange, l_sum, true, l_sum)) ok = false;
         if (ok && !wwait(bar(BAR_O_FINAL), 0)) ok = false;
         if (!ok) {
             fail();
