@@ -59,6 +59,37 @@ def test_step_matches_oracle_chain(idx):
     assert (st == ddtree.DDT_OK).all()
 
 
+def test_split_keys_step_with_flagged_and_underfull_sequences():
+    """With the key range split, the merge kernel also runs the accept walk:
+    a chain (underfull) tree, a full tree, and a sequence whose prefix leaves
+    no room for its nodes (flagged, zero output), against the oracle chain."""
+    from tests.test_gpu_attn import custom_inputs, nan_tail
+    inp = custom_inputs(21, 3, 4, 4, 8, 4, [2500, 1200, 3000], underfull=1)
+    wl = inp.wl
+    inp.prefix_len[2] = inp.Tcap - 2  # T + n_nodes > Tcap
+    ws = ddtree.ddt_workspace_size(wl.B, wl.D, wl.K, wl.budget, wl.H, inp.Tcap)
+    assert ws // (wl.B * wl.Qc * wl.H * 513 * 4) > 1, "the key range must be split"
+    ot = gu.oracle_tree(inp)
+    assert ot.n_nodes[0] < wl.Qc and ot.n_nodes[1] == wl.Qc
+    nan_tail(inp, ot)
+    tg = gu.target_for(inp, ot)
+    step = make_step(inp, tg)
+    step.run()
+    torch.cuda.synchronize()
+    # the tree build passes every sequence; the attention flags the third
+    ot["status"] = ot["status"].copy()
+    ot["status"][2] = ddtree.DDT_E_BADINPUT
+    gu.assert_tree_equal(step.tree, ot)
+    ref = oracle.tree_accept(ot, tg, wl.D)
+    for k in ("accept_len", "accept_idx", "commit_tok", "next_root"):
+        np.testing.assert_array_equal(getattr(step.acc, k).cpu().numpy(), ref[k], err_msg=k)
+    out, lse = step.out.cpu().numpy(), step.lse.cpu().numpy()
+    ref_out, ref_lse = oracle.attn_all(inp.q_lat[:2], inp.q_rope[:2], inp.c_kv[:2], inp.k_rope[:2],
+                                       inp.prefix_len[:2], ot.mask[:2], ot.n_nodes[:2], inp.scale)
+    gu.check_rows(out[:2], lse[:2], ref_out, ref_lse, "split keys, sequences 0-1")
+    assert np.all(out[2] == 0) and np.all(lse[2] == -np.inf)
+
+
 @pytest.mark.parametrize("idx", [1, 2])
 def test_graph_capture_replays_bit_identically(idx):
     inp = synth.make_inputs(idx)
