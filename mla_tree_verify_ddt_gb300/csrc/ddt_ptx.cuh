@@ -412,6 +412,22 @@ __device__ __forceinline__ void sub_f32x2(float a0, float a1, float b0, float b1
         : "=f"(r0), "=f"(r1)
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
+__device__ __forceinline__ void mul_f32x2(float a0, float a1, float b0, float b1, float &r0, float &r1) {
+    asm("{\n\t.reg .b64 a, b, r;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// (a0, a1) * (b0, b1) + (c0, c1)
+__device__ __forceinline__ void fma_f32x2_vv(float a0, float a1, float b0, float b1, float c0, float c1, float &r0,
+                                             float &r1) {
+    asm("{\n\t.reg .b64 a, b, c, r;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 r, a, b, c;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
 // (a0, a1) * c + (d, d)
 __device__ __forceinline__ void fma_f32x2(float a0, float a1, float c, float d, float &r0, float &r1) {
     asm("{\n\t.reg .b64 a, c, d, r;\n\t"

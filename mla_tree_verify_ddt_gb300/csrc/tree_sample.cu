@@ -166,19 +166,32 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
     }
 }
 
-// Weight of logit x against the reference m: 2^((x - m) kd), kd carried as
-// kh + kl with kl > 0 (so x = -inf gives -inf * kl = -inf, weight 0, and a
-// NaN propagates). Every operation is explicitly rounded (no contraction), so
-// the same inputs give the same bits wherever this is evaluated.
-__device__ __forceinline__ float weight(float x, float m, float kh, float kl) {
-    const float d = __fsub_rn(x, m);
-    return ex2_approx(__fmaf_rn(d, kh, __fmul_rn(d, kl)));
+// Weights of two logits x against the reference m: 2^((x - m) kd), kd
+// carried as kh + kl with kl > 0 (so x = -inf gives -inf * kl = -inf, weight
+// 0, and a NaN propagates), computed with packed float32x2 instructions.
+// Every operation is explicitly rounded to nearest (no contraction), so the
+// same inputs give the same bits wherever this is evaluated.
+__device__ __forceinline__ void weight2(float x0, float x1, float m, float kh, float kl, float &e0, float &e1) {
+    float d0, d1, t0, t1, a0, a1;
+    sub_f32x2(x0, x1, m, m, d0, d1);
+    mul_f32x2(d0, d1, kl, kl, t0, t1);
+    fma_f32x2_vv(d0, d1, kh, kh, t0, t1, a0, a1);
+    e0 = ex2_approx(a0);
+    e1 = ex2_approx(a1);
 }
 
 __device__ __forceinline__ float quad_sum(const float4 v, float m, float kh, float kl) {
-    const float e0 = weight(v.x, m, kh, kl), e1 = weight(v.y, m, kh, kl);
-    const float e2 = weight(v.z, m, kh, kl), e3 = weight(v.w, m, kh, kl);
+    float e0, e1, e2, e3;
+    weight2(v.x, v.y, m, kh, kl, e0, e1);
+    weight2(v.z, v.w, m, kh, kl, e2, e3);
     return __fadd_rn(__fadd_rn(__fadd_rn(e0, e1), e2), e3);
+}
+
+// NaN-propagating maximum of three
+__device__ __forceinline__ float max_nan3(float a, float b, float c) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 // 2^((a - b) kd) for a <= b with an exponent good to far below float32
@@ -441,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
             float best = -INFINITY;
 #pragma unroll
             for (int k = 0; k < R; ++k)
-                best = max_nan(best, max_nan(max_nan(x[k].x, x[k].y), max_nan(x[k].z, x[k].w)));
+                best = max_nan3(best, max_nan3(x[k].x, x[k].y, x[k].z), x[k].w);
 #pragma unroll
             for (int o = 16; o; o >>= 1) {
                 best = max_nan(best, __shfl_xor_sync(full, best, o));
@@ -633,8 +646,9 @@ __global__ void __launch_bounds__(kThreads, 2) tree_sample_kernel(const SampleAr
             const float tk = __fsub_rn(tl, kst > 0 ? before : 0.f);
             if (lane == kst) {
                 // element: the float4's own partial sums
-                const float e[4] = {weight(v.x, mr, kh, kl), weight(v.y, mr, kh, kl), weight(v.z, mr, kh, kl),
-                                    weight(v.w, mr, kh, kl)};
+                float e[4];
+                weight2(v.x, v.y, mr, kh, kl, e[0], e[1]);
+                weight2(v.z, v.w, mr, kh, kl, e[2], e[3]);
                 float acc = 0.f;
                 int pick = -1, lastpos = 0;
 #pragma unroll
