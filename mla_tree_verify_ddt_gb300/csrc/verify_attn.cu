@@ -22,34 +22,35 @@
 //    same columns of every KV tile, and computes a partial S (M=128 rows,
 //    N=64 keys, K=288) into tensor memory. Its 256 latent KV columns are also
 //    the V of its half of the output, so O += P V (M=128, N=256, K=64) needs
-//    no further load. Nothing is computed twice and each CTA keeps only part
-//    of Q and half of each KV row (36 KB per 64-key tile) in shared memory,
-//    which leaves room for four KV tiles in flight.
-//  * Tensor memory: O (256 columns), three S buffers of 64 columns, and the
+//    no further load. Nothing is loaded or multiplied twice and each CTA
+//    keeps only part of Q and half of each KV row (36 KB per 64-key tile) in
+//    shared memory, which leaves room for four KV tiles in flight.
+//  * Tensor memory: O (256 columns), three S/P buffers of 64 columns, and the
 //    query's fourth latent chunk plus its rotary part as MMA A operands (the
 //    other three latent chunks are in shared memory). Each thread overwrites
 //    its own lane of S with the P of that tile once it has read S, so S and
 //    P share buffers and a buffer is reused three tiles later, after its PV.
-//  * Rows [64r, 64r+64) are "owned" by CTA r. For each tile the two warps of
-//    the other rows ship their partial-S rows to the partner through
-//    distributed shared memory; the owner warps add the partner's partial to
-//    their own, run the softmax, and ship the probabilities back. Shipping
-//    uses st.async, whose bytes are credited to the receiver's mbarrier on
-//    arrival: a remote store followed by a release-arrive made the sender
-//    wait for the round trip (about 0.8 us). Every row
-//    ends up with P in both CTAs' tensor memory, each CTA multiplies by its
-//    own V half.
-//  * Softmax in fp32, log2 domain, one thread per row, visibility as one
-//    64-bit word per tile (all ones inside the prefix). The reference max
-//    moves lazily: O is rescaled only when a row's max grows by more than 8
-//    (log2 units), so probabilities stay <= 256; the factor travels with P.
+//  * Each softmax thread ships its 32 keys of the CTA's partial S to the
+//    partner with st.async (bytes credited to the partner's mbarrier on
+//    arrival), spread over the softmax of the previous tile, and adds the
+//    partner's partial to its own. Both CTAs then hold the same full S and
+//    run the same softmax, each for its own half of O: no probabilities
+//    cross the cluster.
+//  * Softmax in fp32, log2 domain, two threads per row (warps q and q+4, 32
+//    keys each) that combine their tile max and, at the end, their row sums
+//    through a shared-memory word per row; visibility as one 32-bit word per
+//    half tile (all ones inside the prefix). Scores stay unscaled until the
+//    exponent's FFMA (the scale is positive); packed float32x2 arithmetic.
+//    The reference max moves lazily: O is rescaled only when a row's max
+//    grows by more than 8 (log2 units), so probabilities stay <= 256.
 //  * P goes to the tensor core as two bf16 terms, hi = bf16(p) and
 //    lo = bf16(p - hi), each an A operand from tensor memory against the same
 //    bf16 V; together they carry p to about 2^-17 relative.
 //  * KV rows past the last node may hold anything; the tail tile's V rows
 //    there are zeroed in shared memory before the PV product reads them.
 //  * When the key range is split over several clusters, each writes a
-//    normalised partial and its lse; a second kernel merges them.
+//    normalised partial and its lse; a second kernel merges them (and, inside
+//    the verify step, also runs the accept walk).
 // Every on-chip wait is bounded; on expiry the CTA records DDT_E_TIMEOUT in
 // the sequence's status word, drains its own copies and MMAs and leaves.
 #include <cuda.h>
