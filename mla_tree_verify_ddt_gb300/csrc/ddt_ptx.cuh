@@ -103,16 +103,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
 // Asynchronous store into another CTA's shared memory; when the bytes land
 // they are credited to that CTA's mbarrier (complete_tx). The sender neither
 // waits nor fences: the receiver's barrier, armed with expect_tx for the
@@ -124,30 +114,11 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint4 v, uint3
                  : "memory");
 }
 
-__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
-                 "r"(v), "r"(remote_bar)
-                 : "memory");
-}
-
-// Arrive on a barrier of another CTA of the cluster, releasing this thread's
-// earlier writes (its remote stores included) at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
-                 : "memory");
-}
-
 // Arrive on a barrier of another CTA without ordering this thread's earlier
-// memory accesses. Only for signals whose data dependence is already
-// complete (e.g. "I have read your buffer" sent after the values read were
-// consumed), where a release would also wait for this thread's in-flight
-// remote stores.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
-}
-
-// The same, issued only once `dep` is available: pass a value computed from
-// every word read out of the buffer being handed back. `dep` is first stored
+// memory accesses (a relaxed arrival), issued only once `dep` is available:
+// for signals like "I have read your buffer", where a release would also
+// wait for this thread's in-flight remote stores. Pass as `dep` a value
+// computed from every word read out of the buffer being handed back. `dep` is first stored
 // to a scratch word (a side effect that cannot be dropped, and that cannot
 // issue before all those loads have returned), and instructions issue in
 // order, so the arrive cannot overtake the loads.
@@ -160,12 +131,8 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed_after(uint32_t remote
         : "memory");
 }
 
-// Split whole-cluster barrier. An arriving thread with release semantics
-// first waits for all of its earlier memory operations (global loads
-// included) to be performed; a relaxed arrival orders nothing.
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
+// Split whole-cluster barrier. A relaxed arrival orders nothing (a release
+// one would first wait for all of the thread's earlier memory operations).
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
@@ -211,14 +178,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
-}
-
-// Bring a 2D tile into L2 without touching shared memory.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(m)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
 }
 
 // 3D tile store shared -> global, tracked by this thread's bulk async-group.
@@ -338,17 +297,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
-// One 32-bit column: thread t reads / writes lane (base lane + t).
-__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
-    uint32_t r;
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
-    return r;
-}
-
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-}
-
 // Shared-memory matrix descriptor (tcgen05 format, version 1) for a
 // 128-byte-swizzled operand whose 1024-byte swizzle atoms start 1024-aligned.
 //   lbo: byte stride between atoms along the leading dimension
@@ -448,28 +396,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     // cvt packs its first source into the upper half
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-__device__ __forceinline__ float f16lo_to_f32(uint32_t v) {
-    float f;
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(v));
-    return f;
-}
-__device__ __forceinline__ float f16hi_to_f32(uint32_t v) {
-    float f;
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(v));
-    return f;
-}
-
-// two bf16 (packed) -> two fp16 (packed), round to nearest
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
-    return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
