@@ -186,10 +186,53 @@ def attn_in_struct(q_lat, q_rope, c_kv, k_rope, prefix_len) -> DdtAttnIn:
                      _ptr(k_rope), _ptr(prefix_len))
 
 
-def _contig(*ts):
+_I32, _F32, _BF16 = (torch.int32,), (torch.float32,), (torch.bfloat16,)
+_HALFWORD = (torch.bfloat16, torch.float16, torch.int16)  # moved as raw 2-byte elements
+
+
+def _need(t, name: str, dtypes, shape):
+    """Checks the C ABI cannot make on a raw pointer: element type, shape
+    (None matches any extent) and dense row-major layout. Device memory is
+    checked by _on_device once every argument has passed these."""
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {' or '.join(str(d) for d in dtypes)}")
+    if t.dim() != len(shape) or any(e is not None and e != g for e, g in zip(shape, t.shape)):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected "
+                         f"[{', '.join('*' if e is None else str(e) for e in shape)}]")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: libddtree takes dense row-major tensors")
+
+
+def _on_device(*ts):
     for t in ts:
-        if t is not None and not t.is_contiguous():
-            raise ValueError("libddtree takes dense row-major tensors")
+        if t is not None and not t.is_cuda:
+            raise ValueError("libddtree takes CUDA tensors (device memory)")
+
+
+def _need_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: "Tree"):
+    _need(q_lat, "q_lat", _BF16, (tree.B, tree.Qc, None, LATENT))
+    H = q_lat.shape[2]
+    _need(q_rope, "q_rope", _BF16, (tree.B, tree.Qc, H, ROPE))
+    _need(c_kv, "c_kv", _BF16, (tree.B, None, LATENT))
+    _need(k_rope, "k_rope", _BF16, (tree.B, c_kv.shape[1], ROPE))
+    _need(prefix_len, "prefix_len", _I32, (tree.B,))
+    return H
+
+
+def _need_accept(acc: "Accept", B: int, D: int):
+    _need(acc.accept_len, "accept_len", _I32, (B,))
+    _need(acc.accept_idx, "accept_idx", _I32, (B, D + 1))
+    _need(acc.commit_tok, "commit_tok", _I32, (B, D + 1))
+    _need(acc.next_root, "next_root", _I32, (B,))
+
+
+def _need_out(out, lse, tree: "Tree", H: int, out_dtypes):
+    if out is not None:
+        _need(out, "out", out_dtypes, (tree.B, tree.Qc, H, LATENT))
+    if lse is not None:
+        _need(lse, "lse", _F32, (tree.B, tree.Qc, H))
 
 
 # ------------------------------------------------------------------ calls
@@ -200,8 +243,11 @@ def ddt_workspace_size(B: int, D: int, K: int, budget: int, H: int, Tcap: int) -
 
 def ddt_tree_build(tok, lp, root_tok, budget: int, vocab: int, out: Tree | None = None,
                    stream=None) -> Tree:
-    _contig(tok, lp, root_tok)
-    B, D, _ = tok.shape
+    _need(tok, "tok", _I32, (None, None, None))
+    B, D, K = tok.shape
+    _need(lp, "lp", _F32, (B, D, K))
+    _need(root_tok, "root_tok", _I32, (B,))
+    _on_device(tok, lp, root_tok)
     out = out or Tree.empty(B, D, budget, tok.device)
     d, t = draft_struct(tok, lp, root_tok, vocab), out.c()
     _check(lib().ddt_tree_build(ctypes.byref(d), budget, ctypes.byref(t), _stream_ptr(stream)),
@@ -211,7 +257,8 @@ def ddt_tree_build(tok, lp, root_tok, budget: int, vocab: int, out: Tree | None 
 
 def ddt_verify_mla_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: Tree, scale: float,
                         out=None, lse=None, workspace=None, stream=None):
-    _contig(q_lat, q_rope, c_kv, k_rope, prefix_len)
+    _need_out(out, lse, tree, _need_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree), _F32)
+    _on_device(q_lat, q_rope, c_kv, k_rope, prefix_len, out, lse, workspace)
     B, Qc, H, _ = q_lat.shape
     if out is None:
         out = torch.empty(B, Qc, H, LATENT, dtype=torch.float32, device=q_lat.device)
@@ -233,7 +280,8 @@ def ddt_verify_mla_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: Tree, sca
 def ddt_verify_mla_attn_bf16(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: Tree, scale: float,
                              out=None, lse=None, workspace=None, stream=None):
     """ddt_verify_mla_attn with the latent output in bfloat16."""
-    _contig(q_lat, q_rope, c_kv, k_rope, prefix_len)
+    _need_out(out, lse, tree, _need_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree), _BF16)
+    _on_device(q_lat, q_rope, c_kv, k_rope, prefix_len, out, lse, workspace)
     B, Qc, H, _ = q_lat.shape
     if out is None:
         out = torch.empty(B, Qc, H, LATENT, dtype=torch.bfloat16, device=q_lat.device)
@@ -255,7 +303,14 @@ def ddt_verify_mla_attn_paged(q_lat, q_rope, pool_kv, pool_kr, prefix_len, kv_in
     """Attention on a block-table cache: key position p of sequence b is row
     kv_index[b, p] of pool_kv [P,512] / pool_kr [P,64] (bf16); kv_index is
     int32 [B, Tcap]."""
-    _contig(q_lat, q_rope, pool_kv, pool_kr, prefix_len, kv_index)
+    _need(q_lat, "q_lat", _BF16, (tree.B, tree.Qc, None, LATENT))
+    _need(q_rope, "q_rope", _BF16, (tree.B, tree.Qc, q_lat.shape[2], ROPE))
+    _need(pool_kv, "pool_kv", _BF16, (None, LATENT))
+    _need(pool_kr, "pool_kr", _BF16, (pool_kv.shape[0], ROPE))
+    _need(prefix_len, "prefix_len", _I32, (tree.B,))
+    _need(kv_index, "kv_index", _I32, (tree.B, None))
+    _need_out(out, lse, tree, q_lat.shape[2], _F32)
+    _on_device(q_lat, q_rope, pool_kv, pool_kr, prefix_len, kv_index, out, lse, workspace)
     B, Qc, H, _ = q_lat.shape
     Tcap = kv_index.shape[1]
     if out is None:
@@ -281,7 +336,8 @@ def ddt_verify_mla_attn_noalloc(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: T
     key-range partials go to the library's own fixed device scratch
     (NOALLOC_SCRATCH_BYTES per GPU). Output tensors, if not given, are
     created here by torch; pass them in to allocate nothing at all."""
-    _contig(q_lat, q_rope, c_kv, k_rope, prefix_len)
+    _need_out(out, lse, tree, _need_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree), _F32)
+    _on_device(q_lat, q_rope, c_kv, k_rope, prefix_len, out, lse)
     B, Qc, H, _ = q_lat.shape
     if out is None:
         out = torch.empty(B, Qc, H, LATENT, dtype=torch.float32, device=q_lat.device)
@@ -297,7 +353,11 @@ def ddt_verify_mla_attn_noalloc(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: T
 
 
 def ddt_tree_accept(tree: Tree, target_argmax, out: Accept | None = None, stream=None) -> Accept:
-    _contig(target_argmax)
+    _need(target_argmax, "target_argmax", _I32, (tree.B, tree.Qc))
+    if out is not None:
+        _need_accept(out, tree.B, tree.D)
+        _on_device(out.accept_len, out.accept_idx, out.commit_tok, out.next_root)
+    _on_device(target_argmax)
     out = out or Accept.empty(tree.B, tree.D, target_argmax.device)
     t, a = tree.c(), out.c()
     _check(lib().ddt_tree_accept(ctypes.byref(t), _ptr(target_argmax), ctypes.byref(a),
@@ -310,8 +370,13 @@ def ddt_kv_commit(acc: Accept, c_kv, k_rope, prefix_len, status, stream=None):
     c_kv [B,Tcap,512] and k_rope [B,Tcap,64] (bf16), and advances prefix_len
     (int32 [B]); status (int32 [B]) gets DDT_E_BADINPUT for a sequence whose
     values do not fit."""
-    _contig(c_kv, k_rope, prefix_len, status)
+    _need(c_kv, "c_kv", _HALFWORD, (acc.accept_len.shape[0], None, LATENT))
     B, Tcap, _ = c_kv.shape
+    _need_accept(acc, B, acc.accept_idx.shape[1] - 1)
+    _need(k_rope, "k_rope", _HALFWORD, (B, Tcap, ROPE))
+    _need(prefix_len, "prefix_len", _I32, (B,))
+    _need(status, "status", _I32, (B,))
+    _on_device(c_kv, k_rope, prefix_len, status, acc.accept_len, acc.accept_idx)
     D = acc.accept_idx.shape[1] - 1
     a = acc.c()
     _check(lib().ddt_kv_commit(ctypes.byref(a), B, D, Tcap, _ptr(c_kv), _ptr(k_rope), _ptr(prefix_len),
@@ -324,9 +389,14 @@ def ddt_tree_sample(tree: Tree, logits, temperature: float, u01=None, sample_tok
     [B,Qc,V] (V a multiple of 4), ``u01`` float32 [B,Qc] (not read when
     temperature <= 0, the greedy limit). Returns (sample_tok int32 [B,Qc],
     node_p float32 [B,Qc]); pass sample_tok to ddt_tree_accept as its target."""
-    _contig(logits)
+    _need(logits, "logits", _F32, (tree.B, tree.Qc, None))
     if u01 is not None:
-        _contig(u01)
+        _need(u01, "u01", _F32, (tree.B, tree.Qc))
+    if sample_tok is not None:
+        _need(sample_tok, "sample_tok", _I32, (tree.B, tree.Qc))
+    if node_p is not None:
+        _need(node_p, "node_p", _F32, (tree.B, tree.Qc))
+    _on_device(logits, u01, sample_tok, node_p)
     B, Qc, V = logits.shape
     if sample_tok is None:
         sample_tok = torch.empty(B, Qc, dtype=torch.int32, device=logits.device)
@@ -348,10 +418,18 @@ class VerifyStep:
 
     def __init__(self, tok, lp, root_tok, vocab: int, budget: int, q_lat, q_rope, c_kv, k_rope,
                  prefix_len, target_argmax, scale: float, acc: "Accept | None" = None):
-        _contig(tok, lp, root_tok, q_lat, q_rope, c_kv, k_rope, prefix_len, target_argmax)
+        _need(tok, "tok", _I32, (None, None, None))
         dev = tok.device
         B, D, K = tok.shape
-        H = q_lat.shape[2]
+        _need(lp, "lp", _F32, (B, D, K))
+        _need(root_tok, "root_tok", _I32, (B,))
+        shape = Tree(B, D, budget + 1, 0, *([None] * 10))  # (only B and Qc are read)
+        H = _need_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, shape)
+        _need(target_argmax, "target_argmax", _I32, (B, budget + 1))
+        if acc is not None:
+            _need_accept(acc, B, D)
+            _on_device(acc.accept_len, acc.accept_idx, acc.commit_tok, acc.next_root)
+        _on_device(tok, lp, root_tok, q_lat, q_rope, c_kv, k_rope, prefix_len, target_argmax)
         self.inputs = (tok, lp, root_tok, q_lat, q_rope, c_kv, k_rope, prefix_len, target_argmax)
         self.tree = Tree.empty(B, D, budget, dev)
         self.acc = acc if acc is not None else Accept.empty(B, D, dev)
