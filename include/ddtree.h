@@ -279,12 +279,15 @@ int ddt_tree_sample(const ddt_tree *tree, const float *logits, int vocab, float 
  * file scope: DDT_NOALLOC_SCRATCH_BYTES on every GPU that loads the library,
  * held until the process exits. It allocates nothing.
  *
- *  - Shapes whose key-range partials would not fit return
- *    DDT_E_SCRATCH_LIMIT before anything is enqueued (ddt_workspace_size
- *    tells how much a shape needs on the current device).
- *  - The first call on a device looks up the scratch array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *  - Arguments are checked first, as ddt_verify_mla_attn checks them
+ *    (DDT_E_INVAL, DDT_E_UNSUPPORTED); then shapes whose key-range partials
+ *    would not fit return DDT_E_SCRATCH_LIMIT before anything is enqueued
+ *    (ddt_workspace_size tells how much a shape needs on the current device).
+ *  - The first call on a device whose shape splits its keys looks up the
+ *    scratch array's device address (cudaGetSymbolAddress, with that device
+ *    current); make that first call before any stream capture. Made while
+ *    `stream` is capturing, it returns DDT_E_INVAL and enqueues nothing. A
+ *    failed lookup returns DDT_E_CUDA and is retried by the next call.
  *  - All calls share the one array and it keeps the last call's contents.
  *    Nothing in it needs to start at zero: a call writes every partial it
  *    later reads. Calls whose kernels overlap on the GPU (several streams,

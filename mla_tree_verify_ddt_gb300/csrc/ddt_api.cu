@@ -106,6 +106,17 @@ int check_scale(float scale) { return (scale > 0.f && scale <= FLT_MAX) ? DDT_OK
 
 }  // namespace
 
+namespace ddt {
+int check_attn_call(const ddt_attn_in *in, const ddt_tree *tree, float scale, const ddt_attn_out *out,
+                    AttnPlan *plan) {
+    if (int rc = check_attn(in, tree, out)) return rc;
+    if (int rc = check_scale(scale)) return rc;
+    if (int rc = check_device()) return rc;
+    *plan = plan_attention(tree->B, tree->Qc, in->H, in->Tcap, device_info()->sms);
+    return DDT_OK;
+}
+}  // namespace ddt
+
 extern "C" {
 
 size_t ddt_workspace_size(int B, int D, int K, int budget, int H, int Tcap) {

@@ -38,6 +38,12 @@ struct AttnPlan {
 // Geometry for one attention call on a device with `sms` multiprocessors.
 AttnPlan plan_attention(int B, int Qc, int H, int Tcap, int sms);
 
+// Every host-side check of an attention call (arguments, score scale, an
+// sm_103 current device) and, when they pass, the geometry the launch on
+// the current device will use (ddt_api.cu).
+int check_attn_call(const ddt_attn_in *in, const ddt_tree *tree, float scale, const ddt_attn_out *out,
+                    AttnPlan *plan);
+
 // Encodes the tensor maps and enqueues the attention kernel (and the merge
 // kernel when nsplit > 1). With `fused_accept`, a merge kernel also runs the
 // accept walk in extra blocks of its grid and sets *accepted; without a

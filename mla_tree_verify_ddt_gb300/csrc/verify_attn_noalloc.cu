@@ -15,6 +15,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "ddt_internal.h"
 #include "ddtree.h"
 
 namespace {
@@ -24,33 +25,47 @@ namespace {
 __device__ __align__(256) unsigned char g_noalloc_scratch[DDT_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
+std::mutex g_scratch_mu[kMaxDevices];
+void *g_scratch_ptr[kMaxDevices];  // the array's device address on device d, once looked up
+
+// In host code the array's name only stands in for the device object; its
+// device address comes from cudaGetSymbolAddress with that device current.
+// Only a successful lookup is kept, so a failed one (a transient error) is
+// retried by the next call. The lookup may load the module, which a stream
+// capture in progress would not allow: a first call on a device made while
+// `s` is capturing is refused with DDT_E_INVAL instead.
+int scratch_address(int dev, cudaStream_t s, void **out) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu[dev]);
+    if (!g_scratch_ptr[dev]) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return DDT_E_CUDA;
+        if (cs != cudaStreamCaptureStatusNone) return DDT_E_INVAL;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            (void)cudaGetLastError();  // not sticky: leave no error behind for the caller
+            return DDT_E_CUDA;
+        }
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return DDT_OK;
+}
 
 }  // namespace
 
 extern "C" int ddt_verify_mla_attn_noalloc(const ddt_attn_in *in, const ddt_tree *tree, float scale,
                                            ddt_attn_out *out, void *stream) {
-    if (!in || !tree || !out) return DDT_E_INVAL;
+    // every argument and device check first, then the exact geometry the
+    // launch below uses: its partials must fit the scratch
+    ddt::AttnPlan plan{};
+    if (int rc = ddt::check_attn_call(in, tree, scale, out, &plan)) return rc;
+    if (plan.ws_bytes > DDT_NOALLOC_SCRATCH_BYTES) return DDT_E_SCRATCH_LIMIT;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DDT_E_CUDA;
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return DDT_E_CUDA;
-    if (major * 10 + minor != 103) return DDT_E_UNSUPPORTED;
-    // the scratch this shape needs on this device (0 when the key range is
-    // not split, or when the shape is invalid: the call below rejects those)
-    const size_t need = ddt_workspace_size(tree->B, tree->D, 1, tree->Qc - 1, in->H, in->Tcap);
-    if (need > DDT_NOALLOC_SCRATCH_BYTES) return DDT_E_SCRATCH_LIMIT;
-    // In host code the array's name only stands in for the device object; its
-    // device address comes from cudaGetSymbolAddress, taken once per device
-    // with that device current (the first call on a device does this).
-    std::call_once(g_scratch_once[dev], [dev] {
-        g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_noalloc_scratch);
-    });
-    if (g_scratch_err[dev] != cudaSuccess || !g_scratch_ptr[dev]) return DDT_E_CUDA;
-    return ddt_verify_mla_attn(in, tree, scale, out, g_scratch_ptr[dev], DDT_NOALLOC_SCRATCH_BYTES,
-                               stream);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *scratch = nullptr;
+    if (plan.ws_bytes > 0) {
+        if (int rc = scratch_address(dev, s, &scratch)) return rc;
+    }
+    return ddt::launch_verify_attn(*in, *tree, scale, *out, scratch, DDT_NOALLOC_SCRATCH_BYTES, plan, s);
 }

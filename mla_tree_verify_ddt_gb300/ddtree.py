@@ -205,10 +205,32 @@ def _need(t, name: str, dtypes, shape):
         raise ValueError(f"{name}: libddtree takes dense row-major tensors")
 
 
-def _on_device(*ts):
+def _on_device(*ts, stream=None):
+    """Every tensor in device memory of the current CUDA device, and the
+    stream (if given) on that device too. The C ABI plans the launch for,
+    encodes its tensor maps on, and launches on the current device, so a
+    tensor of another GPU would reach its kernels as a foreign pointer."""
+    cur = None
     for t in ts:
-        if t is not None and not t.is_cuda:
+        if t is None:
+            continue
+        if not t.is_cuda:
             raise ValueError("libddtree takes CUDA tensors (device memory)")
+        if cur is None:
+            cur = torch.cuda.current_device()
+        if t.device.index != cur:
+            raise ValueError(f"tensor on {t.device}, but the current CUDA device is cuda:{cur}: "
+                             "libddtree launches on the current device (torch.cuda.set_device)")
+    if stream is not None:
+        if cur is None:
+            cur = torch.cuda.current_device()
+        if stream.device.index != cur:
+            raise ValueError(f"stream of {stream.device}, but the current CUDA device is cuda:{cur}")
+
+
+def _tree_attn(tree: "Tree"):
+    """The tree tensors the attention reads."""
+    return tree.mask, tree.n_nodes, tree.status
 
 
 def _need_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: "Tree"):
@@ -247,7 +269,7 @@ def ddt_tree_build(tok, lp, root_tok, budget: int, vocab: int, out: Tree | None 
     B, D, K = tok.shape
     _need(lp, "lp", _F32, (B, D, K))
     _need(root_tok, "root_tok", _I32, (B,))
-    _on_device(tok, lp, root_tok)
+    _on_device(tok, lp, root_tok, stream=stream)
     out = out or Tree.empty(B, D, budget, tok.device)
     d, t = draft_struct(tok, lp, root_tok, vocab), out.c()
     _check(lib().ddt_tree_build(ctypes.byref(d), budget, ctypes.byref(t), _stream_ptr(stream)),
@@ -258,7 +280,7 @@ def ddt_tree_build(tok, lp, root_tok, budget: int, vocab: int, out: Tree | None 
 def ddt_verify_mla_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: Tree, scale: float,
                         out=None, lse=None, workspace=None, stream=None):
     _need_out(out, lse, tree, _need_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree), _F32)
-    _on_device(q_lat, q_rope, c_kv, k_rope, prefix_len, out, lse, workspace)
+    _on_device(q_lat, q_rope, c_kv, k_rope, prefix_len, out, lse, workspace, *_tree_attn(tree), stream=stream)
     B, Qc, H, _ = q_lat.shape
     if out is None:
         out = torch.empty(B, Qc, H, LATENT, dtype=torch.float32, device=q_lat.device)
@@ -281,7 +303,7 @@ def ddt_verify_mla_attn_bf16(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: Tree
                              out=None, lse=None, workspace=None, stream=None):
     """ddt_verify_mla_attn with the latent output in bfloat16."""
     _need_out(out, lse, tree, _need_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree), _BF16)
-    _on_device(q_lat, q_rope, c_kv, k_rope, prefix_len, out, lse, workspace)
+    _on_device(q_lat, q_rope, c_kv, k_rope, prefix_len, out, lse, workspace, *_tree_attn(tree), stream=stream)
     B, Qc, H, _ = q_lat.shape
     if out is None:
         out = torch.empty(B, Qc, H, LATENT, dtype=torch.bfloat16, device=q_lat.device)
@@ -310,7 +332,8 @@ def ddt_verify_mla_attn_paged(q_lat, q_rope, pool_kv, pool_kr, prefix_len, kv_in
     _need(prefix_len, "prefix_len", _I32, (tree.B,))
     _need(kv_index, "kv_index", _I32, (tree.B, None))
     _need_out(out, lse, tree, q_lat.shape[2], _F32)
-    _on_device(q_lat, q_rope, pool_kv, pool_kr, prefix_len, kv_index, out, lse, workspace)
+    _on_device(q_lat, q_rope, pool_kv, pool_kr, prefix_len, kv_index, out, lse, workspace, *_tree_attn(tree),
+               stream=stream)
     B, Qc, H, _ = q_lat.shape
     Tcap = kv_index.shape[1]
     if out is None:
@@ -337,7 +360,7 @@ def ddt_verify_mla_attn_noalloc(q_lat, q_rope, c_kv, k_rope, prefix_len, tree: T
     (NOALLOC_SCRATCH_BYTES per GPU). Output tensors, if not given, are
     created here by torch; pass them in to allocate nothing at all."""
     _need_out(out, lse, tree, _need_attn(q_lat, q_rope, c_kv, k_rope, prefix_len, tree), _F32)
-    _on_device(q_lat, q_rope, c_kv, k_rope, prefix_len, out, lse)
+    _on_device(q_lat, q_rope, c_kv, k_rope, prefix_len, out, lse, *_tree_attn(tree), stream=stream)
     B, Qc, H, _ = q_lat.shape
     if out is None:
         out = torch.empty(B, Qc, H, LATENT, dtype=torch.float32, device=q_lat.device)
@@ -357,7 +380,7 @@ def ddt_tree_accept(tree: Tree, target_argmax, out: Accept | None = None, stream
     if out is not None:
         _need_accept(out, tree.B, tree.D)
         _on_device(out.accept_len, out.accept_idx, out.commit_tok, out.next_root)
-    _on_device(target_argmax)
+    _on_device(target_argmax, tree.token, tree.parent, tree.n_nodes, stream=stream)
     out = out or Accept.empty(tree.B, tree.D, target_argmax.device)
     t, a = tree.c(), out.c()
     _check(lib().ddt_tree_accept(ctypes.byref(t), _ptr(target_argmax), ctypes.byref(a),
@@ -376,7 +399,7 @@ def ddt_kv_commit(acc: Accept, c_kv, k_rope, prefix_len, status, stream=None):
     _need(k_rope, "k_rope", _HALFWORD, (B, Tcap, ROPE))
     _need(prefix_len, "prefix_len", _I32, (B,))
     _need(status, "status", _I32, (B,))
-    _on_device(c_kv, k_rope, prefix_len, status, acc.accept_len, acc.accept_idx)
+    _on_device(c_kv, k_rope, prefix_len, status, acc.accept_len, acc.accept_idx, stream=stream)
     D = acc.accept_idx.shape[1] - 1
     a = acc.c()
     _check(lib().ddt_kv_commit(ctypes.byref(a), B, D, Tcap, _ptr(c_kv), _ptr(k_rope), _ptr(prefix_len),
@@ -396,7 +419,8 @@ def ddt_tree_sample(tree: Tree, logits, temperature: float, u01=None, sample_tok
         _need(sample_tok, "sample_tok", _I32, (tree.B, tree.Qc))
     if node_p is not None:
         _need(node_p, "node_p", _F32, (tree.B, tree.Qc))
-    _on_device(logits, u01, sample_tok, node_p)
+    _on_device(logits, u01, sample_tok, node_p, tree.token, tree.parent, tree.n_nodes, tree.status,
+               stream=stream)
     B, Qc, V = logits.shape
     if sample_tok is None:
         sample_tok = torch.empty(B, Qc, dtype=torch.int32, device=logits.device)
@@ -445,8 +469,11 @@ class VerifyStep:
         self._o = DdtAttnOut(_ptr(self.out), _ptr(self.lse))
         self._c = self.acc.c()
         self._tg = _ptr(target_argmax)
+        self._dev = dev.index
 
     def run(self, stream=None):
+        if stream is not None and stream.device.index != self._dev:
+            raise ValueError(f"stream of {stream.device}, but the step's tensors are on cuda:{self._dev}")
         rc = lib().ddt_verify_step(ctypes.byref(self._d), self.budget, ctypes.byref(self._t),
                                    ctypes.byref(self._a), self.scale, ctypes.byref(self._o),
                                    self._tg, ctypes.byref(self._c), _ptr(self.workspace),

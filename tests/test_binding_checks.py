@@ -102,3 +102,26 @@ def test_outputs_and_accept_buffers_are_checked():
     with pytest.raises(TypeError):
         ddtree.ddt_kv_commit(accept(), t(B, TCAP, 512), t(B, TCAP, 64), t(B, dtype=torch.int32),
                              t(B, dtype=torch.int32))
+
+
+class _FakeCuda:
+    """Stands in for a CUDA tensor or stream on device `index` (only the
+    attributes the device check reads)."""
+
+    def __init__(self, index):
+        self.is_cuda = True
+        self.device = torch.device("cuda", index)
+
+
+def test_tensors_of_another_device_are_rejected(monkeypatch):
+    # the library launches on the current device: cuda:0 here
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    ddtree._on_device(_FakeCuda(0), None, _FakeCuda(0), stream=_FakeCuda(0))
+    with pytest.raises(ValueError, match="current CUDA device"):
+        ddtree._on_device(_FakeCuda(0), _FakeCuda(1))
+    with pytest.raises(ValueError, match="current CUDA device"):
+        ddtree._on_device(_FakeCuda(1))
+    with pytest.raises(ValueError, match="stream of cuda:1"):
+        ddtree._on_device(_FakeCuda(0), stream=_FakeCuda(1))
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        ddtree._on_device(_FakeCuda(0), t(3))

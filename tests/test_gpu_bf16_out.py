@@ -56,3 +56,23 @@ def test_bf16_output_against_the_oracle():
                                        ot.n_nodes, inp.scale)
     gu.check_rows(out.float().cpu().numpy().reshape(-1, 512), lse.cpu().numpy().ravel(),
                   ref_out.reshape(-1, 512), ref_lse.ravel(), "bf16 output")
+
+
+@pytest.mark.parametrize("idx", [2, 3])
+def test_bf16_output_against_the_oracle_on_sampled_rows(idx):
+    """Small batch (ragged prefixes) and wide batch (underfull trees), sampled
+    rows against the oracle."""
+    import oracle
+    inp = synth.make_inputs(idx)
+    wl = inp.wl
+    tree = ddtree.ddt_tree_build(gu.i32_dev(inp.draft_tok), gu.f32_dev(inp.draft_lp), gu.i32_dev(inp.root_tok),
+                                 wl.budget, wl.vocab)
+    dev = gu.attn_dev(inp)
+    out, lse = ddtree.ddt_verify_mla_attn_bf16(*dev, tree, inp.scale)
+    torch.cuda.synchronize()
+    ot = gu.oracle_tree(inp)
+    rows = gu.sample_rows(wl.B, wl.Qc, wl.H, ot.n_nodes, seed=60 + idx)
+    ref_out, ref_lse = gu.oracle_rows(inp, ot, rows)
+    o, l = out.float().cpu().numpy(), lse.cpu().numpy()
+    b, i, h = rows[:, 0], rows[:, 1], rows[:, 2]
+    gu.check_rows(o[b, i, h], l[b, i, h], ref_out, ref_lse, f"bf16 output {wl.name}")

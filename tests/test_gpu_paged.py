@@ -91,3 +91,28 @@ def test_bad_entry_below_the_key_end_is_flagged():
                                      inp.scale)
     torch.cuda.synchronize()
     assert tree.status.cpu().numpy()[0] == ddtree.DDT_E_BADINPUT
+
+
+@pytest.mark.parametrize("idx", [1, 2])
+def test_paged_matches_the_oracle_on_sampled_rows(idx):
+    """Single stream (its keys split over many ranges, then merged) and small
+    batch (ragged prefixes), in the launch configuration the benchmark times:
+    sampled rows against the oracle on the gathered cache."""
+    inp = synth.make_inputs(idx)
+    wl = inp.wl
+    ot = gu.oracle_tree(inp)
+    tree = ddtree.ddt_tree_build(gu.i32_dev(inp.draft_tok), gu.f32_dev(inp.draft_lp), gu.i32_dev(inp.root_tok),
+                                 wl.budget, wl.vocab)
+    pool_kv, pool_kr, kvi = paged_inputs(inp, ot.n_nodes, 21 + idx)
+    dev = gu.attn_dev(inp)
+    out, lse = ddtree.ddt_verify_mla_attn_paged(dev[0], dev[1], bf16(pool_kv), bf16(pool_kr), dev[4],
+                                                gu.i32_dev(kvi), tree, inp.scale)
+    torch.cuda.synchronize()
+    assert (tree.status.cpu().numpy() == 0).all()
+    rows = gu.sample_rows(wl.B, wl.Qc, wl.H, ot.n_nodes, seed=40 + idx)
+    gkv, gkr = oracle.gather_paged(pool_kv, pool_kr, kvi)
+    ref_out, ref_lse, _ = oracle.attn_rows(inp.q_lat, inp.q_rope, gkv, gkr, inp.prefix_len, ot.mask, ot.n_nodes,
+                                           inp.scale, rows)
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    b, i, h = rows[:, 0], rows[:, 1], rows[:, 2]
+    gu.check_rows(o[b, i, h], l[b, i, h], ref_out, ref_lse, f"paged {wl.name}")
