@@ -36,10 +36,11 @@
 //    partner's partial to its own. Both CTAs then hold the same full S and
 //    run the same softmax, each for its own half of O: no probabilities
 //    cross the cluster.
-//  * Softmax in fp32, log2 domain, two threads per row (warps q and q+4, 32
-//    keys each) that combine their tile max and, at the end, their row sums
-//    through a shared-memory word per row; visibility as one 32-bit word per
-//    half tile (all ones inside the prefix). Scores stay unscaled until the
+//  * Softmax in fp32, log2 domain, two threads per row: lanes t and t+16 of
+//    one warp read the same tensor-memory lane (the 16x32bx2 access shape),
+//    32 keys each, and combine their tile max and, at the end, their row sums
+//    with one shuffle; visibility as one 32-bit word per half tile (all ones
+//    inside the prefix). Scores stay unscaled until the
 //    exponent's FFMA (the scale is positive); packed float32x2 arithmetic.
 //    The reference max moves lazily: O is rescaled only when a row's max
 //    grows by more than 8 (log2 units), so probabilities stay <= 256.
@@ -88,11 +89,8 @@ constexpr int kOffBar = kOffSX + kSXBytes;                        // 229376: bar
 constexpr int kOffTree = kOffBar + 272;                           // 229648: the tree as this CTA needs it
 constexpr int kMaxTileNodes = DDT_MAX_BUDGET + 1;                 // nodes a 128-row tile can span (<= Qc)
 constexpr int kTreeBytes = 16 + kMaxTileNodes * 16;               // node count, then 2 mask words per node
-constexpr int kOffXRow = kOffTree + kTreeBytes;                   // 230704: one float per row, the two
-                                                                  // threads of a row combine through it
-constexpr int kSmemBytes = kOffXRow + kRows * 4 + 1024;           // + alignment slack
+constexpr int kSmemBytes = kOffTree + kTreeBytes + 1024;          // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-static_assert(kOffXRow % 16 == 0, "row words aligned");
 constexpr int kOutBoxBytes = kRows * 128;                         // output staging: 128 rows x 32 fp32
 static_assert(8 * kOutBoxBytes <= kSlots * kSlotBytes, "output staging must fit in the KV ring");
 
@@ -105,10 +103,13 @@ constexpr uint32_t kColQR = 480;    // 16: rotary query (bf16 pairs)
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// warps 0-7 softmax group (two threads per row), 8 TMA producer, 9 MMA issuer,
-// 10 tree fetch (it waits for the tree build, which stalls its whole warp)
-constexpr int kThreads = 352;
-constexpr int kProducerWarp = 8, kMmaWarp = 9, kTreeWarp = 10;
+// warps 0-7 softmax group (two threads per row), 8 TMA producer, 9 S-MMA
+// issuer (and tensor-memory owner), 10 tree fetch (it waits for the tree
+// build, which stalls its whole warp), 11 PV-MMA issuer. A thread issues one
+// tcgen05.mma every ~46 cycles at most, which is slower than an N=64 S MMA
+// executes; two issuing threads keep the tensor pipe fed (S and PV share it).
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kTreeWarp = 10, kPvWarp = 11;
 
 enum {
     BAR_Q_FULL = 0,
@@ -119,17 +120,13 @@ enum {
     BAR_P_FULL = 13,     // kSPBufs
     BAR_PV_DONE = 16,    // kSPBufs
     BAR_O_FINAL = 19,
-    BAR_DRAIN = 20,
+    BAR_DRAIN = 20,      // the S issuer's MMAs, after a failure
     // exchange barriers, arrived on by the partner CTA's threads
     BAR_SX_FULL = 21,    // partner's partial S of the tile is in my SX
     BAR_SX_EMPTY = 22,   // partner has read the partial S I wrote into its SX
-    // the two threads of a row combine their halves' tile max (and, at the
-    // end, their row sums), per TMEM lane quadrant: XA the key-half-1 warp's
-    // value is in shared memory, XB the combined value is
-    BAR_XA = 23,         // 4
-    BAR_TREE = 27,       // the tree's node count and this tile's node masks are in shared memory
-    BAR_XB = 28,         // 4
-    NUM_BARS = 32        // (one per lane of the initialising warp)
+    BAR_TREE = 23,       // the tree's node count and this tile's node masks are in shared memory
+    BAR_DRAIN_PV = 24,   // the PV issuer's MMAs, after a failure
+    NUM_BARS = 25        // (one per lane of the initialising warp)
 };
 
 // arrival count of barrier i (see the enum); with a block-table cache the
@@ -189,7 +186,8 @@ __device__ __noinline__ uint32_t half_tile_visibility(int key0, int T, int n, ui
 }
 
 // The epilogue's staging of one thread's 128 output columns (tensor-memory
-// columns o_col .. o_col+127 of its lane, times inv_l, or zeros) in the KV
+// columns o_col + 128 half .. +127 of its lane, read with the 16x32bx2 shape
+// whose second range starts 128 columns on; times inv_l, or zeros) in the KV
 // ring as the boxes the tensor store reads: four 128-row x 32-column float32
 // boxes, or two 128-row x 64-column bfloat16 boxes (rounded to nearest even),
 // in the 128-byte swizzle (16-byte group j of row r at j ^ (r % 8)). Written
@@ -202,7 +200,7 @@ __device__ __noinline__ void stage_output(uint32_t o_col, uint8_t *ring, int hal
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
-            tmem_ld32(o_col + c * 32, o);
+            tmem_ld16x2_32<128>(o_col + c * 32, o);
             tmem_wait_ld();
             uint8_t *box_row = ring + (half * 4 + c) * kOutBoxBytes + row * 128;
 #pragma unroll
@@ -219,7 +217,7 @@ __device__ __noinline__ void stage_output(uint32_t o_col, uint8_t *ring, int hal
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
             uint32_t o[32];
-            tmem_ld32(o_col + cc * 32, o);
+            tmem_ld16x2_32<128>(o_col + cc * 32, o);
             tmem_wait_ld();
             uint8_t *box_row = ring + (half * 2 + (cc >> 1)) * kOutBoxBytes + row * 128;
 #pragma unroll
@@ -491,73 +489,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(BAR_TREE));
         if (a.kv_index) gather_keys(32);  // ======== KV gather, keys 32-63 of each tile
     } else if (warp == kMmaWarp) {
-        // ======================= MMA issuer =======================
+        // ======================= S issuer =======================
+        // S_j = Q K_j^T (this CTA's half of the contraction) into S/P buffer
+        // j % kSPBufs, once the buffer's previous PV (tile j - kSPBufs) is done
+        // and KV tile j is in the ring.
         if (lane == 0) {
             constexpr uint32_t idS = idesc_f32acc(kRows, kKeys, 1, 0, 0);   // bf16 Q, K (K-major)
-            constexpr uint32_t idPV = idesc_f32acc(kRows, 256, 1, 0, 1);  // bf16 P (TMEM), V (MN-major)
             bool ok = mbar_wait(bar(BAR_Q_FULL), 0, deadline, abort_flag) &&
                       mbar_wait(bar(BAR_QT_READY), 0, deadline, abort_flag);
             tc_fence_after();
-            int pv_next = 0;  // the next tile whose PV is still to be issued
-            // O += P_j V_j (both bf16 terms of P) once P_j is in tensor memory.
-            // With block == false it only issues when P_j is already there.
-            auto issue_pv = [&](int j, bool block) -> int {
-                const int pb = j % kSPBufs;
-                if (block) {
-                    if (!mbar_wait(bar(BAR_P_FULL + pb), (j / kSPBufs) & 1, deadline, abort_flag)) return -1;
-                } else if (!mbar_try_wait(bar(BAR_P_FULL + pb), (j / kSPBufs) & 1)) {
-                    return 0;
-                }
-                tc_fence_after();
-                const int slot = j % kSlots;
-                const uint32_t vb = sRing + slot * kSlotBytes;
-                // keys 32c..32c+31 of P sit in columns 32c..32c+31 of the
-                // buffer: 16 hi words, then 16 lo words
-                const uint32_t pcol = tmem + kColSP + pb * 64;
-                for (int ks = 0; ks < kKeys / 16; ++ks)
-                    mma_ts(tmem + kColO, pcol + (ks >> 1) * 32 + (ks & 1) * 8,
-                           desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV, (j > 0 || ks > 0) ? 1u : 0u);
-                for (int ks = 0; ks < kKeys / 16; ++ks)
-                    mma_ts(tmem + kColO, pcol + (ks >> 1) * 32 + 16 + (ks & 1) * 8,
-                           desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV, 1u);
-                mma_commit(bar(BAR_PV_DONE + pb));
-                mma_commit(bar(BAR_RING_EMPTY + slot));
-                return 1;
-            };
-            auto try_pv = [&]() -> bool {
-                if (pv_next >= nrange) return true;
-                const int r = issue_pv(pv_next, false);
-                if (r < 0) return false;
-                pv_next += r;
-                return true;
-            };
-            // Wait for a barrier phase, issuing any PV (up to tile `upto`)
-            // whose P becomes ready meanwhile: the ring and the S/P buffers
-            // are freed by PVs, so an idle issuer must not sit on a ready one.
-            auto wait_feeding_pv = [&](uint32_t barrier, uint32_t parity, int upto) -> bool {
-                for (uint32_t it = 0;; ++it) {
-                    if (mbar_try_wait(barrier, parity)) return true;
-                    if (pv_next < upto && pv_next < nrange) {
-                        const int r = issue_pv(pv_next, false);
-                        if (r < 0) return false;
-                        pv_next += r;
-                    }
-                    if ((it & 63u) == 63u && (*abort_flag || globaltimer_ns() > deadline)) return false;
-                }
-            };
             for (int jj = 0; jj < nrange && ok; ++jj) {
                 const int sb = jj % kSPBufs, slot = jj % kSlots;
-                // a PV that became ready goes first
-                if (pv_next < jj && !try_pv()) {
-                    ok = false;
-                    break;
-                }
-                // the S/P buffer of tile jj-3 is free once its PV is done
-                if (jj >= kSPBufs && !wait_feeding_pv(bar(BAR_PV_DONE + sb), ((jj - kSPBufs) / kSPBufs) & 1, jj)) {
-                    ok = false;
-                    break;
-                }
-                if (!wait_feeding_pv(bar(BAR_RING_FULL + slot), (jj / kSlots) & 1, jj)) {
+                if ((jj >= kSPBufs && !mbar_wait(bar(BAR_PV_DONE + sb), ((jj - kSPBufs) / kSPBufs) & 1, deadline,
+                                                 abort_flag)) ||
+                    !mbar_wait(bar(BAR_RING_FULL + slot), (jj / kSlots) & 1, deadline, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -579,21 +524,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mma_ts(dS, tmem + kColQR + ks * 8, desc_sw64(kb + kQChunks * kChunkBytesKV + ks * 32, 512), idS,
                            1u);
                 mma_commit(bar(BAR_S_FULL + sb));
-                // P of a tile arrives after the next tile's S has gone round
-                // the cluster, so PV may trail S by up to two tiles; only
-                // then does the issuer wait for it
-                while (ok && pv_next < jj - 1) {
-                    if (issue_pv(pv_next, true) < 0) ok = false;
-                    else ++pv_next;
-                }
             }
-            while (ok && pv_next < nrange) {
-                if (issue_pv(pv_next, true) < 0) ok = false;
-                else ++pv_next;
-            }
-            if (ok) {
-                mma_commit(bar(BAR_O_FINAL));
-            } else {
+            if (!ok) {
                 fail();
                 // wait for this thread's MMAs before tensor memory is released
                 mma_commit(bar(BAR_DRAIN));
@@ -601,17 +533,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_wait(bar(BAR_DRAIN), 0, globaltimer_ns() + 100000000ull, &zero);
             }
         }
+    } else if (warp == kPvWarp) {
+        // ======================= PV issuer =======================
+        // O += P_j V_j (both bf16 terms of P) once P_j is in tensor memory;
+        // then S/P buffer j % kSPBufs and ring slot j % kSlots are free.
+        if (lane == 0) {
+            constexpr uint32_t idPV = idesc_f32acc(kRows, 256, 1, 0, 1);  // bf16 P (TMEM), V (MN-major)
+            bool ok = true;
+            for (int j = 0; j < nrange && ok; ++j) {
+                const int pb = j % kSPBufs, slot = j % kSlots;
+                if (!mbar_wait(bar(BAR_P_FULL + pb), (j / kSPBufs) & 1, deadline, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t vb = sRing + slot * kSlotBytes;
+                // keys 32c..32c+31 of P sit in columns 32c..32c+31 of the
+                // buffer: 16 hi words, then 16 lo words
+                const uint32_t pcol = tmem + kColSP + pb * 64;
+                for (int ks = 0; ks < kKeys / 16; ++ks)
+                    mma_ts(tmem + kColO, pcol + (ks >> 1) * 32 + (ks & 1) * 8,
+                           desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV, (j > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < kKeys / 16; ++ks)
+                    mma_ts(tmem + kColO, pcol + (ks >> 1) * 32 + 16 + (ks & 1) * 8,
+                           desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV, 1u);
+                mma_commit(bar(BAR_PV_DONE + pb));
+                mma_commit(bar(BAR_RING_EMPTY + slot));
+            }
+            if (ok) {
+                mma_commit(bar(BAR_O_FINAL));
+            } else {
+                fail();
+                mma_commit(bar(BAR_DRAIN_PV));
+                const int zero = 0;
+                mbar_wait(bar(BAR_DRAIN_PV), 0, globaltimer_ns() + 100000000ull, &zero);
+            }
+        }
     } else {
         // ======================= softmax group (warps 0-7) =======================
-        // Warp w serves tensor-memory lanes 32(w%4)..+31 (one row per lane)
-        // and key half c = w/4 of every tile: keys [32c, 32c+32). Per tile a
-        // thread ships its partial S to the partner, adds the partner's
-        // partial to its own, and runs the softmax of its row and key half.
-        // Both CTAs then hold the same full S and compute the same P (fp32
-        // addition commutes), each for its own half of O. The two threads of
-        // a row agree on the row max through shared memory.
-        const int quad = warp & 3, half = warp >> 2;
-        const int row = quad * 32 + lane;            // TMEM lane of this thread
+        // Warp w serves 16 rows: tensor-memory lanes 32(w%4) + 16(w/4) ..
+        // +15 of its lane quadrant. Lanes t and t+16 share a row and take its
+        // key halves c = t/16 of every tile, keys [32c, 32c+32), through the
+        // 16x32bx2 access shape. Per tile a thread ships its partial S to the
+        // partner, adds the partner's partial to its own, and runs the
+        // softmax of its row and key half. Both CTAs then hold the same full S
+        // and compute the same P (fp32 addition commutes), each for its own
+        // half of O. The two threads of a row agree on the row max with a
+        // shuffle.
+        const int quad = warp & 3, sub = warp >> 2, half = lane >> 4;
+        const int row = quad * 32 + sub * 16 + (lane & 15);   // TMEM lane of this thread
         const int g = mt * kRows + row;              // row within the sequence
         const bool row_in_seq = g < rows_seq;
         const int node = g / a.H;
@@ -632,8 +602,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             return ready;
         };
-        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t col_half = static_cast<uint32_t>(half) * 32;   // this thread's 32 columns of an S/P buffer
+        // this warp's 16 lanes; the S/P buffer columns of key half 1 start 32
+        // columns on, those of O's second half 128 columns on
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32 + sub * 16) << 16;
         const uint4 *sx = reinterpret_cast<const uint4 *>(smem + kOffSX);   // [16 groups][128 rows] of 4 floats
         const uint32_t r_sx = mapa_shared(sbase + kOffSX, peer);
         const uint32_t r_bar_sx_full = mapa_shared(bar(BAR_SX_FULL), peer);
@@ -649,37 +620,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto wwait_cluster = [&](uint32_t barrier, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait_cluster(barrier, parity, deadline, abort_flag));
         };
-        // The two threads of a row (warps q and q+4) combine one float each
-        // round k through the row's shared-memory word: the key-half-1 thread
-        // writes its value, the key-half-0 thread reads it, combines (max or
-        // sum) and writes the result back, which the key-half-1 thread then
-        // reads; each hand-off is phase k of a barrier of the quadrant. The
-        // word is rewritten only after its last reader has arrived on the
-        // barrier the next writer waits for, so one word per row suffices.
-        float *xrow = reinterpret_cast<float *>(smem + kOffXRow) + row;
-        auto combine_halves = [&](int k, float v, bool sum, float &r) -> bool {
-            if (half == 1) {
-                *xrow = v;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BAR_XA + quad));
-                if (!wwait(bar(BAR_XB + quad), k & 1)) return false;
-                r = *xrow;
-            } else {
-                if (!wwait(bar(BAR_XA + quad), k & 1)) return false;
-                const float o = *xrow;
-                r = sum ? v + o : fmaxf(v, o);
-                *xrow = r;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BAR_XB + quad));
-            }
-            return true;
-        };
-
-        // this row's latent query chunk 3 (key-half-0 warps) or rotary query
-        // (key-half-1 warps) -> tensor memory, as bf16 pairs (low half = even column)
+        // the latent query chunk 3 (warps 0-3) or rotary query (warps 4-7) of
+        // the 32 rows of lane quadrant w % 4 -> tensor memory, one row per
+        // lane, as bf16 pairs (low half = even column)
         {
-            if (half == 0) tmem_st32(tmem + lane_base + kColQ3, q_pre);
-            else tmem_st16(tmem + lane_base + kColQR, *reinterpret_cast<const uint32_t(*)[16]>(&q_pre[0]));
+            const uint32_t quad_base = static_cast<uint32_t>(quad * 32) << 16;
+            if (sub == 0) tmem_st32(tmem + quad_base + kColQ3, q_pre);
+            else tmem_st16(tmem + quad_base + kColQR, *reinterpret_cast<const uint32_t(*)[16]>(&q_pre[0]));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -692,7 +639,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!wwait(bar(BAR_S_FULL + buf), par)) return false;
             __syncwarp();
             tc_fence_after();
-            tmem_ld32(tmem + lane_base + kColSP + buf * 64 + col_half, sv);
+            tmem_ld16x2_32<32>(tmem + lane_base + kColSP + buf * 64, sv);
             tmem_wait_ld();
             return true;
         };
@@ -792,11 +739,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mxa = fmax3(mxa, s[k], s[k + 1]);
                 mxb = fmax3(mxb, s[k + 2], s[k + 3]);
             }
-            float mx = fmaxf(mxa, mxb) * a.scale_log2;
-            if (!combine_halves(jj, mx, false, mx)) {
-                ok = false;
-                break;
-            }
+            float mx = fmaxf(mxa, mxb);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * a.scale_log2;  // the row's other key half
             float alpha = 1.0f;  // rescale factor of this row's O for this tile
             if (mx > m_ref + kRescaleThreshold) {
                 alpha = ex2_approx(m_ref - mx);  // 0 while nothing was visible before
@@ -832,13 +776,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
-                    const uint32_t col = kColO + half * 128 + c * 32;
+                    const uint32_t col = kColO + c * 32;  // (+128 for key half 1)
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + col, o);
+                    tmem_ld16x2_32<128>(tmem + lane_base + col, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int v = 0; v < 32; ++v) o[v] = __float_as_uint(__uint_as_float(o[v]) * alpha);
-                    tmem_st32(tmem + lane_base + col, o);
+                    tmem_st16x2_32<128>(tmem + lane_base + col, o);
                 }
             }
             // KV rows past the last node may hold anything (NaN included) and
@@ -852,7 +796,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (((e >> 3) & (kKeys - 1)) >= kvalid) vset[e] = make_uint4(0, 0, 0, 0);
                 fence_proxy_async_smem();
             }
-            tmem_st32(tmem + lane_base + kColSP + sb * 64 + col_half, pw);
+            tmem_st16x2_32<32>(tmem + lane_base + kColSP + sb * 64, pw);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -863,7 +807,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (ok && !resolved && !resolve_s()) ok = false;
         // the row sum is the two halves' sums (same reference max)
         float l_sum = l_even + l_odd;
-        if (ok && !combine_halves(nrange, l_sum, true, l_sum)) ok = false;
+        l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 16);
         if (ok && !wwait(bar(BAR_O_FINAL), 0)) ok = false;
         if (!ok) {
             fail();
@@ -876,7 +820,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const float inv_l = (l_sum > 0.f && !zero_row) ? 1.0f / l_sum : 0.f;
             // stage this thread's 128 output columns in the KV ring (idle
             // once every PV is done) for the tensor store
-            stage_output(tmem + lane_base + kColO + half * 128, smem + kOffRing, half, row, zero_row, inv_l,
+            stage_output(tmem + lane_base + kColO, smem + kOffRing, half, row, zero_row, inv_l,
                          a.out_bf16 != 0);
             fence_proxy_async_smem();
             // both CTAs hold the same row sum and max; one writes the lse
