@@ -333,16 +333,16 @@ class Bench:
         return g
 
     def timed(self, graph, n, before=None):
-        """n replays, each after an L2-evicting write (and `before`, if
-        given) outside its CUDA-event window; returns the event pairs."""
+        """n replays, each after an L2-evicting write and then `before`, if
+        given, both outside its CUDA-event window; returns the event pairs."""
         torch, s = self.torch, self.s
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
         with torch.cuda.stream(s):
             for e0, e1 in evs:
+                self.flush.fill_(1)
                 if before is not None:
                     before()
-                self.flush.fill_(1)
                 e0.record(s)
                 graph.replay()
                 e1.record(s)
