@@ -108,6 +108,22 @@ def test_full_parity_many_key_range_chunks(seed, T, lo, hi):
     full_check(inp, f"{nsplit} key-range chunks")
 
 
+@pytest.mark.parametrize("seed,B,T", [
+    (11, 5, [100, 3000, 40, 2000, 700]),      # prefix lengths far apart
+    (12, 7, [4000, 4000, 1, 4000, 63, 64, 65]),
+])
+def test_full_parity_ragged_prefixes_over_row_tiles(seed, B, T):
+    """Ragged prefixes over several row tiles per sequence (9 nodes x 20
+    heads = 2 row tiles): every sequence's key ranges are cut from its own
+    prefix length on the device, so ranges of different lengths, ranges
+    past a short sequence's keys and the merge of split ranges all occur."""
+    inp = custom_inputs(seed, B, 4, 4, 8, 20, T)
+    wl = inp.wl
+    ws = ddtree.ddt_workspace_size(B, wl.D, wl.K, wl.budget, wl.H, inp.Tcap)
+    assert ws > 0, "the key range must be split"
+    full_check(inp, f"ragged prefixes, seed {seed}")
+
+
 @pytest.mark.parametrize("idx", [2, 3, 4])
 def test_sampled_parity_large_workloads(idx):
     inp = synth.make_inputs(idx)
