@@ -185,52 +185,45 @@ __device__ __noinline__ uint32_t half_tile_visibility(int key0, int T, int n, ui
     return vis;
 }
 
-// The epilogue's staging of one thread's 128 output columns (tensor-memory
-// columns o_col + 128 half .. +127 of its lane, read with the 16x32bx2 shape
-// whose second range starts 128 columns on; times inv_l, or zeros) in the KV
-// ring as the boxes the tensor store reads: four 128-row x 32-column float32
-// boxes, or two 128-row x 64-column bfloat16 boxes (rounded to nearest even),
-// in the 128-byte swizzle (16-byte group j of row r at j ^ (r % 8)). Written
-// this way each warp store is conflict-free, where direct row-strided global
-// stores cost a transaction per lane. Out of line, so its temporaries do not
-// weigh on the register allocation of the kernel's main loop.
-__device__ __noinline__ void stage_output(uint32_t o_col, uint8_t *ring, int half, int row, bool zero_row,
-                                          float inv_l, bool bf16) {
+// The epilogue's staging of one 32-column chunk c (0..3) of a thread's 128
+// output columns (tensor-memory columns o_col + 128 half + 32c .. +31 of its
+// lane, read with the 16x32bx2 shape whose second range starts 128 columns
+// on; times inv_l, or zeros) in the KV ring as the boxes the tensor store
+// reads: 128-row x 32-column float32 boxes (box 4 half + c), or 128-row x
+// 64-column bfloat16 boxes (box 2 half + c/2, its half c%2), rounded to
+// nearest even, in the 128-byte swizzle (16-byte group j of row r at
+// j ^ (r % 8)). Written this way each warp store is conflict-free, where
+// direct row-strided global stores cost a transaction per lane. Out of line,
+// so its temporaries do not weigh on the register allocation of the kernel's
+// main loop.
+__device__ __noinline__ void stage_chunk(uint32_t o_col, uint8_t *ring, int half, int row, bool zero_row,
+                                         float inv_l, bool bf16, int c) {
+    uint32_t o[32];
+    tmem_ld16x2_32<128>(o_col + c * 32, o);
+    tmem_wait_ld();
     if (!bf16) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld16x2_32<128>(o_col + c * 32, o);
-            tmem_wait_ld();
-            uint8_t *box_row = ring + (half * 4 + c) * kOutBoxBytes + row * 128;
+        uint8_t *box_row = ring + (half * 4 + c) * kOutBoxBytes + row * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 v = zero_row ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                          : make_float4(__uint_as_float(o[4 * j]) * inv_l,
-                                                        __uint_as_float(o[4 * j + 1]) * inv_l,
-                                                        __uint_as_float(o[4 * j + 2]) * inv_l,
-                                                        __uint_as_float(o[4 * j + 3]) * inv_l);
-                *reinterpret_cast<float4 *>(box_row + ((j ^ (row & 7)) << 4)) = v;
-            }
+        for (int j = 0; j < 8; ++j) {
+            const float4 v = zero_row ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                      : make_float4(__uint_as_float(o[4 * j]) * inv_l,
+                                                    __uint_as_float(o[4 * j + 1]) * inv_l,
+                                                    __uint_as_float(o[4 * j + 2]) * inv_l,
+                                                    __uint_as_float(o[4 * j + 3]) * inv_l);
+            *reinterpret_cast<float4 *>(box_row + ((j ^ (row & 7)) << 4)) = v;
         }
     } else {
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t o[32];
-            tmem_ld16x2_32<128>(o_col + cc * 32, o);
-            tmem_wait_ld();
-            uint8_t *box_row = ring + (half * 2 + (cc >> 1)) * kOutBoxBytes + row * 128;
+        uint8_t *box_row = ring + (half * 2 + (c >> 1)) * kOutBoxBytes + row * 128;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t w[4];
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    w[v] = zero_row ? 0u
-                                    : pack_bf16x2(__uint_as_float(o[8 * j + 2 * v]) * inv_l,
-                                                  __uint_as_float(o[8 * j + 2 * v + 1]) * inv_l);
-                const int grp = (cc & 1) * 4 + j;
-                *reinterpret_cast<uint4 *>(box_row + ((grp ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
+            for (int v = 0; v < 4; ++v)
+                w[v] = zero_row ? 0u
+                                : pack_bf16x2(__uint_as_float(o[8 * j + 2 * v]) * inv_l,
+                                              __uint_as_float(o[8 * j + 2 * v + 1]) * inv_l);
+            const int grp = (c & 1) * 4 + j;
+            *reinterpret_cast<uint4 *>(box_row + ((grp ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
 }
@@ -419,8 +412,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         cp_async_wait_all();  // every copy has landed before the CTA can leave
     };
 
-    float *lse_out = nullptr;  // set by the softmax threads that write an lse
-    float lse_val = 0.f;
+    bool stored = false;  // this thread issued tensor stores of the output block
     if (nrange <= 0) {
         // nothing visible in this range: zero rows (this CTA's half), lse = -inf
         // (this CTA's 256 columns of a row: 64 float4, or 32 uint4 of bfloat16)
@@ -809,31 +801,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float l_sum = l_even + l_odd;
         l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 16);
         if (ok && !wwait(bar(BAR_O_FINAL), 0)) ok = false;
-        if (!ok) {
-            fail();
-        } else {
-            __syncwarp();
-            tc_fence_after();
-            // rows of absent nodes, and every row of a range with no tile of
-            // this sequence's keys, are zero (tensor memory was not written)
-            const bool zero_row = !node_ok;
-            const float inv_l = (l_sum > 0.f && !zero_row) ? 1.0f / l_sum : 0.f;
-            // stage this thread's 128 output columns in the KV ring (idle
-            // once every PV is done) for the tensor store
-            stage_output(tmem + lane_base + kColO, smem + kOffRing, half, row, zero_row, inv_l,
-                         a.out_bf16 != 0);
+        if (!ok) fail();
+        __syncwarp();
+        tc_fence_after();
+        // This thread's remote operations are over (the last partial shipped,
+        // the last exchange buffer handed back; a release arrival orders them
+        // first): arrive on the cluster barrier that lets the partner leave.
+        // It is waited on only at the very end, so the staging and stores
+        // below hold neither CTA. (Arriving right after the tile loop instead
+        // measured 0.9% slower on the max-budget workload.)
+        cluster_arrive_release();
+        // rows of absent nodes, and every row of a range with no tile of
+        // this sequence's keys, are zero (tensor memory was not written)
+        const bool zero_row = !node_ok;
+        const float inv_l = (l_sum > 0.f && !zero_row) ? 1.0f / l_sum : 0.f;
+        // Stage this thread's 128 output columns in the KV ring (idle once
+        // every PV is done), 32 at a time; as soon as the eight softmax warps
+        // have staged a chunk, one thread stores the boxes it completes, so
+        // the stores overlap the rest of the staging. The tensor map has the
+        // sequence's rows as one dimension: rows past the sequence are not
+        // written. Every softmax warp takes part in each barrier, failed or
+        // not (a failure is in the abort flag before the first one).
+        const int box_cols = a.out_bf16 ? 64 : 32;
+        for (int c = 0; c < 4; ++c) {
+            if (ok) stage_chunk(tmem + lane_base + kColO, smem + kOffRing, half, row, zero_row, inv_l,
+                                a.out_bf16 != 0, c);
             fence_proxy_async_smem();
-            // both CTAs hold the same row sum and max; one writes the lse
-            // (after the final cluster barrier, like the output block)
-            if (rank == 0 && half == 0 && row_in_seq) {
-                lse_out = lse_dst + row_base + g;
-                lse_val = (l_sum > 0.f && !zero_row) ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+            named_bar_sync(1, 8 * 32);
+            if (tid == 0 && !*abort_flag && (!a.out_bf16 || (c & 1))) {
+                // float32: boxes c and 4 + c; bfloat16: boxes c/2 and 2 + c/2
+                const int box0 = a.out_bf16 ? (c >> 1) : c, box1 = box0 + (a.out_bf16 ? 2 : 4);
+                tma_store_3d(&tm_o, sRing + box0 * kOutBoxBytes, static_cast<int>(rank) * 256 + box0 * box_cols,
+                             mt * kRows, b + a.B * chunk);
+                tma_store_3d(&tm_o, sRing + box1 * kOutBoxBytes, static_cast<int>(rank) * 256 + box1 * box_cols,
+                             mt * kRows, b + a.B * chunk);
+                bulk_commit_group();
+                stored = true;
             }
         }
+        // both CTAs hold the same row sum and max; one writes the lse
+        if (ok && rank == 0 && half == 0 && row_in_seq)
+            lse_dst[row_base + g] =
+                (l_sum > 0.f && !zero_row) ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
     }
 
-    // (threads that did not wait on the setup's cluster barrier do it now)
-    if (warp >= kProducerWarp || nrange <= 0) cluster_wait();
+    // The other threads wait on the setup's cluster barrier now and arrive
+    // on the final one (they made no remote access).
+    if (warp >= kProducerWarp || nrange <= 0) {
+        cluster_wait();
+        cluster_arrive_relaxed();
+    }
     // Every thread has waited for the tree build by now (or does so here);
     // only then may the next kernel of the step start.
     grid_dep_wait();
@@ -850,31 +867,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (!seq_ok && mt == 0 && rank == 0 && chunk == 0 && !*abort_flag) a.status[b] = DDT_E_BADINPUT;
     }
+    // every tensor-memory access of the CTA is complete before it is freed
     tc_fence_before();
-    // Neither CTA may leave while its partner can still write into it. The
-    // output block and the lse are stored after this barrier, so its release
-    // arrivals do not wait for them (measured: a tensor store issued before
-    // it held the barrier about 2.5 us).
-    cluster_sync();
-    // every softmax warp has staged its part of the output block (the
-    // barrier above orders that for the whole CTA): one thread stores the
-    // CTA's 128 x 256 block; the tensor map has the sequence's rows as one
-    // dimension, so rows past the sequence are not written
-    const bool store_out = tid == 0 && nrange > 0 && !*abort_flag;
-    if (store_out) {
-        // eight float32 boxes of 32 columns, or four bfloat16 boxes of 64
-        const int nbox = a.out_bf16 ? 4 : 8, box_cols = a.out_bf16 ? 64 : 32;
-        for (int c = 0; c < nbox; ++c)
-            tma_store_3d(&tm_o, sRing + c * kOutBoxBytes, static_cast<int>(rank) * 256 + c * box_cols, mt * kRows,
-                         b + a.B * chunk);
-        bulk_commit_group();
-    }
+    __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (lse_out) *lse_out = lse_val;
-    if (store_out) bulk_wait_read_all();
+    // the tensor stores have read the staged block before shared memory is
+    // released, and neither CTA leaves while its partner can still access it
+    if (stored) bulk_wait_read_all();
+    cluster_wait();
 }
 
 // Merge per-chunk normalised partials: lse = log sum_c exp(lse_c),
