@@ -108,6 +108,23 @@ def test_full_parity_many_key_range_chunks(seed, T, lo, hi):
     full_check(inp, f"{nsplit} key-range chunks")
 
 
+@pytest.mark.parametrize("seed,B,H,T,lo,hi", [
+    (13, 1, 4, [16000], 33, 64),      # one tile, more than 32 chunks (two lse values per merge lane)
+    (14, 20, 1, [4000] * 20, 5, 8),   # many sequences, 8 early loads
+    (15, 16, 1, [8000] * 16, 9, 16),  # many sequences, 16 early loads
+])
+def test_full_parity_merge_of_many_chunks(seed, B, H, T, lo, hi):
+    """The merge of split key ranges with more than 32 chunks of one
+    sequence's keys, and with many sequences at once, against the oracle on
+    every row."""
+    inp = custom_inputs(seed, B, 4, 4, 8, H, T)
+    wl = inp.wl
+    ws = ddtree.ddt_workspace_size(B, wl.D, wl.K, wl.budget, wl.H, inp.Tcap)
+    nsplit = ws // (B * wl.Qc * wl.H * 513 * 4)
+    assert lo <= nsplit <= hi, f"{nsplit} key-range chunks"
+    full_check(inp, f"{B} sequences, {nsplit} key-range chunks")
+
+
 @pytest.mark.parametrize("seed,B,T", [
     (11, 5, [100, 3000, 40, 2000, 700]),      # prefix lengths far apart
     (12, 7, [4000, 4000, 1, 4000, 63, 64, 65]),
