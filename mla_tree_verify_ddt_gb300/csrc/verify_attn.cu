@@ -487,6 +487,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // and KV tile j is in the ring.
         if (lane == 0) {
             constexpr uint32_t idS = idesc_f32acc(kRows, kKeys, 1, 0, 0);   // bf16 Q, K (K-major)
+            // operand descriptors of the query's chunk 0 and of ring slot 0's
+            // latent chunk 0 and rotary part; the loop adds offsets / 16
+            const uint64_t dq = desc_sw128(sQ, 16, 1024), dk = desc_sw128(sRing, 16, 1024),
+                           dr = desc_sw64(sRing + kQChunks * kChunkBytesKV, 512);
+            const uint32_t dq_lo = static_cast<uint32_t>(dq), dq_hi = static_cast<uint32_t>(dq >> 32);
+            const uint32_t dk_lo = static_cast<uint32_t>(dk), dk_hi = static_cast<uint32_t>(dk >> 32);
+            const uint32_t dr_lo = static_cast<uint32_t>(dr), dr_hi = static_cast<uint32_t>(dr >> 32);
             bool ok = mbar_wait(bar(BAR_Q_FULL), 0, deadline, abort_flag) &&
                       mbar_wait(bar(BAR_QT_READY), 0, deadline, abort_flag);
             tc_fence_after();
@@ -503,18 +510,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (a.kv_index) fence_proxy_async_smem();
                 tc_fence_after();
                 const uint32_t dS = tmem + kColSP + sb * 64;
-                const uint32_t kb = sRing + slot * kSlotBytes;
+                const uint32_t k_lo = dk_lo + ((slot * kSlotBytes) >> 4), r_lo = dr_lo + ((slot * kSlotBytes) >> 4);
+#pragma unroll
                 for (int c = 0; c < kQSmemChunks; ++c)
+#pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ss(dS, desc_sw128(sQ + c * kChunkBytesQ + ks * 32, 16, 1024),
-                               desc_sw128(kb + c * kChunkBytesKV + ks * 32, 16, 1024), idS,
-                               (c > 0 || ks > 0) ? 1u : 0u);
+                        mma_ss_w(dS, dq_lo + ((c * kChunkBytesQ + ks * 32) >> 4), dq_hi,
+                                 k_lo + ((c * kChunkBytesKV + ks * 32) >> 4), dk_hi, idS, (c > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_ts(dS, tmem + kColQ3 + ks * 8, desc_sw128(kb + 3 * kChunkBytesKV + ks * 32, 16, 1024), idS,
-                           1u);
+                    mma_ts_w(dS, tmem + kColQ3 + ks * 8, k_lo + ((3 * kChunkBytesKV + ks * 32) >> 4), dk_hi, idS, 1u);
+#pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
-                    mma_ts(dS, tmem + kColQR + ks * 8, desc_sw64(kb + kQChunks * kChunkBytesKV + ks * 32, 512), idS,
-                           1u);
+                    mma_ts_w(dS, tmem + kColQR + ks * 8, r_lo + ((ks * 32) >> 4), dr_hi, idS, 1u);
                 mma_commit(bar(BAR_S_FULL + sb));
             }
             if (!ok) {
@@ -531,6 +539,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // then S/P buffer j % kSPBufs and ring slot j % kSlots are free.
         if (lane == 0) {
             constexpr uint32_t idPV = idesc_f32acc(kRows, 256, 1, 0, 1);  // bf16 P (TMEM), V (MN-major)
+            // ring slot 0's V descriptor; the loop adds offsets / 16
+            const uint64_t dv = desc_sw128(sRing, kChunkBytesKV, 1024);
+            const uint32_t dv_lo = static_cast<uint32_t>(dv), dv_hi = static_cast<uint32_t>(dv >> 32);
             bool ok = true;
             for (int j = 0; j < nrange && ok; ++j) {
                 const int pb = j % kSPBufs, slot = j % kSlots;
@@ -539,16 +550,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t vb = sRing + slot * kSlotBytes;
+                const uint32_t v_lo = dv_lo + ((slot * kSlotBytes) >> 4);
                 // keys 32c..32c+31 of P sit in columns 32c..32c+31 of the
                 // buffer: 16 hi words, then 16 lo words
                 const uint32_t pcol = tmem + kColSP + pb * 64;
+#pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    mma_ts(tmem + kColO, pcol + (ks >> 1) * 32 + (ks & 1) * 8,
-                           desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV, (j > 0 || ks > 0) ? 1u : 0u);
+                    mma_ts_w(tmem + kColO, pcol + (ks >> 1) * 32 + (ks & 1) * 8, v_lo + ((ks * 2048) >> 4), dv_hi, idPV,
+                             (j > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    mma_ts(tmem + kColO, pcol + (ks >> 1) * 32 + 16 + (ks & 1) * 8,
-                           desc_sw128(vb + ks * 2048, kChunkBytesKV, 1024), idPV, 1u);
+                    mma_ts_w(tmem + kColO, pcol + (ks >> 1) * 32 + 16 + (ks & 1) * 8, v_lo + ((ks * 2048) >> 4), dv_hi,
+                             idPV, 1u);
                 mma_commit(bar(BAR_PV_DONE + pb));
                 mma_commit(bar(BAR_RING_EMPTY + slot));
             }
