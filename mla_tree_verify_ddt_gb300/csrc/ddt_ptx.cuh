@@ -95,6 +95,17 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     }
 }
 
+// One lane of the (fully active) warp gets true.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(e));
+    return e != 0;
+}
+
 // ---------------------------------------------------------------- cluster / DSMEM
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

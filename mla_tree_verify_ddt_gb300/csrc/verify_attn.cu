@@ -484,33 +484,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ======================= S issuer =======================
         // S_j = Q K_j^T (this CTA's half of the contraction) into S/P buffer
         // j % kSPBufs, once the buffer's previous PV (tile j - kSPBufs) is done
-        // and KV tile j is in the ring.
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_f32acc(kRows, kKeys, 1, 0, 0);   // bf16 Q, K (K-major)
-            // operand descriptors of the query's chunk 0 and of ring slot 0's
-            // latent chunk 0 and rotary part; the loop adds offsets / 16
-            const uint64_t dq = desc_sw128(sQ, 16, 1024), dk = desc_sw128(sRing, 16, 1024),
-                           dr = desc_sw64(sRing + kQChunks * kChunkBytesKV, 512);
-            const uint32_t dq_lo = static_cast<uint32_t>(dq), dq_hi = static_cast<uint32_t>(dq >> 32);
-            const uint32_t dk_lo = static_cast<uint32_t>(dk), dk_hi = static_cast<uint32_t>(dk >> 32);
-            const uint32_t dr_lo = static_cast<uint32_t>(dr), dr_hi = static_cast<uint32_t>(dr >> 32);
-            bool ok = mbar_wait(bar(BAR_Q_FULL), 0, deadline, abort_flag) &&
-                      mbar_wait(bar(BAR_QT_READY), 0, deadline, abort_flag);
+        // and KV tile j is in the ring. The whole warp runs the loop, so its
+        // operands stay warp-uniform; one elected lane issues the MMAs and
+        // commits.
+        const bool leader = elect_one();
+        constexpr uint32_t idS = idesc_f32acc(kRows, kKeys, 1, 0, 0);   // bf16 Q, K (K-major)
+        // operand descriptors of the query's chunk 0 and of ring slot 0's
+        // latent chunk 0 and rotary part; the loop adds offsets / 16
+        const uint64_t dq = desc_sw128(sQ, 16, 1024), dk = desc_sw128(sRing, 16, 1024),
+                       dr = desc_sw64(sRing + kQChunks * kChunkBytesKV, 512);
+        const uint32_t dq_lo = static_cast<uint32_t>(dq), dq_hi = static_cast<uint32_t>(dq >> 32);
+        const uint32_t dk_lo = static_cast<uint32_t>(dk), dk_hi = static_cast<uint32_t>(dk >> 32);
+        const uint32_t dr_lo = static_cast<uint32_t>(dr), dr_hi = static_cast<uint32_t>(dr >> 32);
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q_FULL), 0, deadline, abort_flag) &&
+                                              mbar_wait(bar(BAR_QT_READY), 0, deadline, abort_flag));
+        tc_fence_after();
+        for (int jj = 0; jj < nrange && ok; ++jj) {
+            const int sb = jj % kSPBufs, slot = jj % kSlots;
+            if (!__all_sync(0xffffffffu, (jj < kSPBufs || mbar_wait(bar(BAR_PV_DONE + sb), ((jj - kSPBufs) / kSPBufs) & 1,
+                                                                   deadline, abort_flag)) &&
+                                             mbar_wait(bar(BAR_RING_FULL + slot), (jj / kSlots) & 1, deadline,
+                                                       abort_flag))) {
+                ok = false;
+                break;
+            }
+            // gathered tiles were written by ordinary (generic-proxy)
+            // copies: order them before the tensor core's reads
+            if (a.kv_index) fence_proxy_async_smem();
             tc_fence_after();
-            for (int jj = 0; jj < nrange && ok; ++jj) {
-                const int sb = jj % kSPBufs, slot = jj % kSlots;
-                if ((jj >= kSPBufs && !mbar_wait(bar(BAR_PV_DONE + sb), ((jj - kSPBufs) / kSPBufs) & 1, deadline,
-                                                 abort_flag)) ||
-                    !mbar_wait(bar(BAR_RING_FULL + slot), (jj / kSlots) & 1, deadline, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                // gathered tiles were written by ordinary (generic-proxy)
-                // copies: order them before the tensor core's reads
-                if (a.kv_index) fence_proxy_async_smem();
-                tc_fence_after();
-                const uint32_t dS = tmem + kColSP + sb * 64;
-                const uint32_t k_lo = dk_lo + ((slot * kSlotBytes) >> 4), r_lo = dr_lo + ((slot * kSlotBytes) >> 4);
+            const uint32_t dS = tmem + kColSP + sb * 64;
+            const uint32_t k_lo = dk_lo + ((slot * kSlotBytes) >> 4), r_lo = dr_lo + ((slot * kSlotBytes) >> 4);
+            if (leader) {
 #pragma unroll
                 for (int c = 0; c < kQSmemChunks; ++c)
 #pragma unroll
@@ -525,35 +529,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mma_ts_w(dS, tmem + kColQR + ks * 8, r_lo + ((ks * 32) >> 4), dr_hi, idS, 1u);
                 mma_commit(bar(BAR_S_FULL + sb));
             }
-            if (!ok) {
-                fail();
-                // wait for this thread's MMAs before tensor memory is released
-                mma_commit(bar(BAR_DRAIN));
-                const int zero = 0;
-                mbar_wait(bar(BAR_DRAIN), 0, globaltimer_ns() + 100000000ull, &zero);
-            }
+            __syncwarp();
+        }
+        if (!ok && leader) {
+            fail();
+            // wait for this thread's MMAs before tensor memory is released
+            mma_commit(bar(BAR_DRAIN));
+            const int zero = 0;
+            mbar_wait(bar(BAR_DRAIN), 0, globaltimer_ns() + 100000000ull, &zero);
         }
     } else if (warp == kPvWarp) {
         // ======================= PV issuer =======================
         // O += P_j V_j (both bf16 terms of P) once P_j is in tensor memory;
-        // then S/P buffer j % kSPBufs and ring slot j % kSlots are free.
-        if (lane == 0) {
-            constexpr uint32_t idPV = idesc_f32acc(kRows, 256, 1, 0, 1);  // bf16 P (TMEM), V (MN-major)
-            // ring slot 0's V descriptor; the loop adds offsets / 16
-            const uint64_t dv = desc_sw128(sRing, kChunkBytesKV, 1024);
-            const uint32_t dv_lo = static_cast<uint32_t>(dv), dv_hi = static_cast<uint32_t>(dv >> 32);
-            bool ok = true;
-            for (int j = 0; j < nrange && ok; ++j) {
-                const int pb = j % kSPBufs, slot = j % kSlots;
-                if (!mbar_wait(bar(BAR_P_FULL + pb), (j / kSPBufs) & 1, deadline, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t v_lo = dv_lo + ((slot * kSlotBytes) >> 4);
-                // keys 32c..32c+31 of P sit in columns 32c..32c+31 of the
-                // buffer: 16 hi words, then 16 lo words
-                const uint32_t pcol = tmem + kColSP + pb * 64;
+        // then S/P buffer j % kSPBufs and ring slot j % kSlots are free. The
+        // whole warp runs the loop; one elected lane issues and commits.
+        const bool leader = elect_one();
+        constexpr uint32_t idPV = idesc_f32acc(kRows, 256, 1, 0, 1);  // bf16 P (TMEM), V (MN-major)
+        // ring slot 0's V descriptor; the loop adds offsets / 16
+        const uint64_t dv = desc_sw128(sRing, kChunkBytesKV, 1024);
+        const uint32_t dv_lo = static_cast<uint32_t>(dv), dv_hi = static_cast<uint32_t>(dv >> 32);
+        bool ok = true;
+        for (int j = 0; j < nrange && ok; ++j) {
+            const int pb = j % kSPBufs, slot = j % kSlots;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_P_FULL + pb), (j / kSPBufs) & 1, deadline, abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t v_lo = dv_lo + ((slot * kSlotBytes) >> 4);
+            // keys 32c..32c+31 of P sit in columns 32c..32c+31 of the
+            // buffer: 16 hi words, then 16 lo words
+            const uint32_t pcol = tmem + kColSP + pb * 64;
+            if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks)
                     mma_ts_w(tmem + kColO, pcol + (ks >> 1) * 32 + (ks & 1) * 8, v_lo + ((ks * 2048) >> 4), dv_hi, idPV,
@@ -565,6 +572,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mma_commit(bar(BAR_PV_DONE + pb));
                 mma_commit(bar(BAR_RING_EMPTY + slot));
             }
+            __syncwarp();
+        }
+        if (leader) {
             if (ok) {
                 mma_commit(bar(BAR_O_FINAL));
             } else {
