@@ -76,23 +76,33 @@ constexpr int kQSmemChunks = 3;     // query chunks 0-2 in shared memory; chunk 
 constexpr int kChunkBytesQ = kRows * 128;    // 64 bf16 x 128 rows, 128-byte swizzle
 constexpr int kChunkBytesKV = kKeys * 128;   // 64 bf16 x 64 keys
 constexpr int kKRopeBytes = kKeys * 64;      // 32 bf16 x 64 keys, 64-byte swizzle
-constexpr int kSlotBytes = kQChunks * kChunkBytesKV + kKRopeBytes;  // 36864
-constexpr int kSlots = 4;           // KV tiles in flight
+constexpr int kLatBytes = kQChunks * kChunkBytesKV;  // 32768: a tile's latent keys (and its V)
+constexpr int kTileBytes = kLatBytes + kKRopeBytes;  // 36864: a tile's bytes in shared memory
+constexpr int kSlots = 4;           // latent KV tiles in flight
 constexpr int kSPBufs = 3;          // S / P buffers in tensor memory
+constexpr int kRopeSlots = kSPBufs; // rotary key tiles in flight: the slot of tile j (j % 3) is
+                                    // free again once S of tile j - 3 is done
+// The partner's partial S arrives in units of one key half of a tile (128
+// rows x 32 keys), each score the top 24 bits of its float32 pattern, rounded:
+// 12 KB a unit, in a ring of three units (tile j's key half h is unit 2j + h,
+// slot (2j + h) % 3), so a tile's partial can travel while the previous
+// one is still being read.
+constexpr int kSXUnitBytes = kRows * 32 * 3;  // 12288
+constexpr int kSXUnits = 3;
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffQ = 0;
-constexpr int kOffRing = kOffQ + kQSmemChunks * kChunkBytesQ;     // 49152
-constexpr int kOffSX = kOffRing + kSlots * kSlotBytes;            // 196608: the partner's partial S of a tile
-constexpr int kSXBytes = kRows * kKeys * 4;                       // 32768
-constexpr int kOffBar = kOffSX + kSXBytes;                        // 229376: barriers and flags (272 B)
+constexpr int kOffRing = kOffQ + kQSmemChunks * kChunkBytesQ;     // 49152: latent ring
+constexpr int kOffRope = kOffRing + kSlots * kLatBytes;           // 180224: rotary ring
+constexpr int kOffSX = kOffRope + kRopeSlots * kKRopeBytes;       // 192512: exchange ring
+constexpr int kOffBar = kOffSX + kSXUnits * kSXUnitBytes;         // 229376: barriers and flags (272 B)
 constexpr int kOffTree = kOffBar + 272;                           // 229648: the tree as this CTA needs it
 constexpr int kMaxTileNodes = DDT_MAX_BUDGET + 1;                 // nodes a 128-row tile can span (<= Qc)
 constexpr int kTreeBytes = 16 + kMaxTileNodes * 16;               // node count, then 2 mask words per node
 constexpr int kSmemBytes = kOffTree + kTreeBytes + 1024;          // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 constexpr int kOutBoxBytes = kRows * 128;                         // output staging: 128 rows x 32 fp32
-static_assert(8 * kOutBoxBytes <= kSlots * kSlotBytes, "output staging must fit in the KV ring");
+static_assert(8 * kOutBoxBytes <= kSlots * kLatBytes, "output staging must fit in the latent ring");
 
 // tensor memory columns
 constexpr uint32_t kColO = 0;       // 256: this CTA's half of O
@@ -105,11 +115,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // warps 0-7 softmax group (two threads per row), 8 TMA producer, 9 S-MMA
 // issuer (and tensor-memory owner), 10 tree fetch (it waits for the tree
-// build, which stalls its whole warp), 11 PV-MMA issuer. A thread issues one
-// tcgen05.mma every ~46 cycles at most, which is slower than an N=64 S MMA
-// executes; two issuing threads keep the tensor pipe fed (S and PV share it).
-constexpr int kThreads = 384;
-constexpr int kProducerWarp = 8, kMmaWarp = 9, kTreeWarp = 10, kPvWarp = 11;
+// build, which stalls its whole warp), 11 PV-MMA issuer, 12-15 partial-S
+// shippers (warp 12 + q: rows 32q..32q+31, its tensor-memory lane quadrant).
+// A thread issues one tcgen05.mma every ~46 cycles at most, which is slower
+// than an N=64 S MMA executes; two issuing threads keep the tensor pipe fed
+// (S and PV share it).
+constexpr int kThreads = 512;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kTreeWarp = 10, kPvWarp = 11, kShipWarp0 = 12;
 
 enum {
     BAR_Q_FULL = 0,
@@ -121,20 +133,23 @@ enum {
     BAR_PV_DONE = 16,    // kSPBufs
     BAR_O_FINAL = 19,
     BAR_DRAIN = 20,      // the S issuer's MMAs, after a failure
-    // exchange barriers, arrived on by the partner CTA's threads
-    BAR_SX_FULL = 21,    // partner's partial S of the tile is in my SX
-    BAR_SX_EMPTY = 22,   // partner has read the partial S I wrote into its SX
-    BAR_TREE = 23,       // the tree's node count and this tile's node masks are in shared memory
-    BAR_DRAIN_PV = 24,   // the PV issuer's MMAs, after a failure
-    NUM_BARS = 25        // (one per lane of the initialising warp)
+    BAR_TREE = 21,       // the tree's node count and this tile's node masks are in shared memory
+    BAR_DRAIN_PV = 22,   // the PV issuer's MMAs, after a failure
+    BAR_S_READ = 23,     // kSPBufs: the shippers have read S of the buffer (P may overwrite it)
+    // exchange ring, one barrier per unit slot
+    BAR_SX_FULL = 26,    // kSXUnits: the partner's unit is in my slot (its bytes come from the partner)
+    BAR_SX_EMPTY = 29,   // kSXUnits: the partner has read the unit my shippers wrote into its slot
+    NUM_BARS = 32        // (one per lane of the initialising warp)
 };
+static_assert(kRopeSlots == kSPBufs, "a rotary slot is released by the S_FULL barrier of the same index");
 
 // arrival count of barrier i (see the enum); with a block-table cache the
 // ring is filled by the 64 lanes of two gather warps instead of TMA
 __device__ __forceinline__ uint32_t bar_count(int i, bool gathered) {
     if (gathered && i >= BAR_RING_FULL && i < BAR_RING_FULL + kSlots) return 64;  // two gather warps
     if (i == BAR_QT_READY || (i >= BAR_P_FULL && i < BAR_P_FULL + kSPBufs)) return 8;  // one per softmax warp
-    if (i == BAR_SX_EMPTY) return 2 * kRows;  // every partner softmax thread
+    if (i >= BAR_S_READ && i < BAR_S_READ + kSPBufs) return 4;                          // one per shipper warp
+    if (i >= BAR_SX_EMPTY && i < BAR_SX_EMPTY + kSXUnits) return kRows;  // the partner's threads of one key half
     return 1;  // one arrival (SX_FULL: the arming thread; its bytes come from the partner's st.async)
 }
 
@@ -228,6 +243,29 @@ __device__ __noinline__ void stage_chunk(uint32_t o_col, uint8_t *ring, int half
     }
 }
 
+// Partial scores cross the cluster as the top 24 bits of their float32
+// patterns, rounded to nearest (adding 0x80 carries a low byte of 0x80 or more
+// into them): four scores in three words. Word k of a run of rounded patterns
+// r[0..]: bytes 1-3 of r[4g], then of r[4g+1], ... packed low byte first.
+__device__ __forceinline__ uint32_t pack24_word(const uint32_t *r, int k) {
+    const int g = 4 * (k / 3);
+    switch (k % 3) {
+        case 0: return __byte_perm(r[g] + 0x80u, r[g + 1] + 0x80u, 0x5321);
+        case 1: return __byte_perm(r[g + 1] + 0x80u, r[g + 2] + 0x80u, 0x6532);
+        default: return __byte_perm(r[g + 2] + 0x80u, r[g + 3] + 0x80u, 0x7653);
+    }
+}
+// The four rounded float32 patterns (low byte zero) packed in w0, w1, w2.
+__device__ __forceinline__ void unpack24(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t (&v)[4]) {
+    v[0] = __byte_perm(w0, 0u, 0x2104);
+    v[1] = __byte_perm(w0, w1, 0x5430) & 0xFFFFFF00u;
+    v[2] = __byte_perm(w1, w2, 0x4320) & 0xFFFFFF00u;
+    v[3] = w2 & 0xFFFFFF00u;
+}
+// The same rounding of a pattern the CTA keeps (its own partial), so both
+// CTAs add the same two rounded terms.
+__device__ __forceinline__ uint32_t round24(uint32_t x) { return (x + 0x80u) & 0xFFFFFF00u; }
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                        const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_o,
@@ -274,7 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + kOffQ, sRing = sbase + kOffRing;
+    const uint32_t sQ = sbase + kOffQ, sRing = sbase + kOffRing, sRope = sbase + kOffRope;
     const uint32_t sBar = sbase + kOffBar;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + NUM_BARS * 8 + 4);
@@ -374,13 +412,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int32_t *kvi = a.kv_index + static_cast<size_t>(b) * a.Tcap;
         bool ok = true, bad_index = false;
         for (int jj = 0; jj < nrange; ++jj) {
-            const int slot = jj % kSlots, use = jj / kSlots;
-            if (use >= 1 &&
-                !__all_sync(0xffffffffu, mbar_wait(bar(BAR_RING_EMPTY + slot), (use - 1) & 1, deadline, abort_flag))) {
+            const int slot = jj % kSlots, use = jj / kSlots, rs = jj % kRopeSlots;
+            if (!__all_sync(0xffffffffu,
+                            (use < 1 || mbar_wait(bar(BAR_RING_EMPTY + slot), (use - 1) & 1, deadline, abort_flag)) &&
+                                (jj < kRopeSlots || mbar_wait(bar(BAR_S_FULL + rs), ((jj - kRopeSlots) / kRopeSlots) & 1,
+                                                              deadline, abort_flag)))) {
                 ok = false;
                 break;
             }
-            const uint32_t dst = sRing + slot * kSlotBytes;
+            const uint32_t dst = sRing + slot * kLatBytes, rdst = sRope + rs * kKRopeBytes;
             // pool row of key k_lo + lane of the tile
             const int key = (t0 + jj) * kKeys + k_lo + lane;
             int phys = key < a.Tcap ? kvi[key] : 0;
@@ -402,7 +442,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int i0 = 0; i0 < 32; i0 += 8) {
                 const int i = i0 + (lane >> 2), q = lane & 3, r = k_lo + i;
                 const int pr = __shfl_sync(0xffffffffu, phys, i);
-                cp_async_16(dst + kQChunks * kChunkBytesKV + r * 64 + ((q ^ ((r >> 1) & 3)) << 4),
+                cp_async_16(rdst + r * 64 + ((q ^ ((r >> 1) & 3)) << 4),
                             a.pool_kr + static_cast<size_t>(pr) * 128 + rank * 64 + q * 16);
             }
             cp_async_arrive_noinc(bar(BAR_RING_FULL + slot));
@@ -441,19 +481,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int armed[kSlots] = {0, 0, 0, 0};
             bool ok = true;
             for (int jj = 0; jj < nrange; ++jj) {
-                const int slot = jj % kSlots, use = jj / kSlots;
-                if (use >= 1 && !mbar_wait(bar(BAR_RING_EMPTY + slot), (use - 1) & 1, deadline, abort_flag)) {
+                const int slot = jj % kSlots, use = jj / kSlots, rs = jj % kRopeSlots;
+                // latent slot: PV of tile jj - 4 done; rotary slot: S of tile jj - 3 done
+                if ((use >= 1 && !mbar_wait(bar(BAR_RING_EMPTY + slot), (use - 1) & 1, deadline, abort_flag)) ||
+                    (jj >= kRopeSlots &&
+                     !mbar_wait(bar(BAR_S_FULL + rs), ((jj - kRopeSlots) / kRopeSlots) & 1, deadline, abort_flag))) {
                     ok = false;
                     break;
                 }
                 const int key_row = b * a.Tcap + (t0 + jj) * kKeys;
-                const uint32_t dst = sRing + slot * kSlotBytes;
-                mbar_arrive_expect_tx(bar(BAR_RING_FULL + slot), kSlotBytes);
+                const uint32_t dst = sRing + slot * kLatBytes;
+                mbar_arrive_expect_tx(bar(BAR_RING_FULL + slot), kTileBytes);
                 ++armed[slot];
                 for (int c = 0; c < kQChunks; ++c)
                     tma_load_2d(dst + c * kChunkBytesKV, &tm_kv, static_cast<int>(rank) * 256 + c * 64, key_row,
                                 bar(BAR_RING_FULL + slot));
-                tma_load_2d(dst + kQChunks * kChunkBytesKV, &tm_kr, static_cast<int>(rank) * 32, key_row,
+                tma_load_2d(sRope + rs * kKRopeBytes, &tm_kr, static_cast<int>(rank) * 32, key_row,
                             bar(BAR_RING_FULL + slot));
             }
             if (!ok) {
@@ -489,10 +532,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // commits.
         const bool leader = elect_one();
         constexpr uint32_t idS = idesc_f32acc(kRows, kKeys, 1, 0, 0);   // bf16 Q, K (K-major)
-        // operand descriptors of the query's chunk 0 and of ring slot 0's
-        // latent chunk 0 and rotary part; the loop adds offsets / 16
-        const uint64_t dq = desc_sw128(sQ, 16, 1024), dk = desc_sw128(sRing, 16, 1024),
-                       dr = desc_sw64(sRing + kQChunks * kChunkBytesKV, 512);
+        // operand descriptors of the query's chunk 0, of latent slot 0's
+        // chunk 0 and of rotary slot 0; the loop adds offsets / 16
+        const uint64_t dq = desc_sw128(sQ, 16, 1024), dk = desc_sw128(sRing, 16, 1024), dr = desc_sw64(sRope, 512);
         const uint32_t dq_lo = static_cast<uint32_t>(dq), dq_hi = static_cast<uint32_t>(dq >> 32);
         const uint32_t dk_lo = static_cast<uint32_t>(dk), dk_hi = static_cast<uint32_t>(dk >> 32);
         const uint32_t dr_lo = static_cast<uint32_t>(dr), dr_hi = static_cast<uint32_t>(dr >> 32);
@@ -513,7 +555,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (a.kv_index) fence_proxy_async_smem();
             tc_fence_after();
             const uint32_t dS = tmem + kColSP + sb * 64;
-            const uint32_t k_lo = dk_lo + ((slot * kSlotBytes) >> 4), r_lo = dr_lo + ((slot * kSlotBytes) >> 4);
+            const uint32_t k_lo = dk_lo + ((slot * kLatBytes) >> 4), r_lo = dr_lo + ((sb * kKRopeBytes) >> 4);
             if (leader) {
 #pragma unroll
                 for (int c = 0; c < kQSmemChunks; ++c)
@@ -545,7 +587,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // whole warp runs the loop; one elected lane issues and commits.
         const bool leader = elect_one();
         constexpr uint32_t idPV = idesc_f32acc(kRows, 256, 1, 0, 1);  // bf16 P (TMEM), V (MN-major)
-        // ring slot 0's V descriptor; the loop adds offsets / 16
+        // latent slot 0's V descriptor; the loop adds offsets / 16
         const uint64_t dv = desc_sw128(sRing, kChunkBytesKV, 1024);
         const uint32_t dv_lo = static_cast<uint32_t>(dv), dv_hi = static_cast<uint32_t>(dv >> 32);
         bool ok = true;
@@ -556,7 +598,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t v_lo = dv_lo + ((slot * kSlotBytes) >> 4);
+            const uint32_t v_lo = dv_lo + ((slot * kLatBytes) >> 4);
             // keys 32c..32c+31 of P sit in columns 32c..32c+31 of the
             // buffer: 16 hi words, then 16 lo words
             const uint32_t pcol = tmem + kColSP + pb * 64;
@@ -584,17 +626,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_wait(bar(BAR_DRAIN_PV), 0, globaltimer_ns() + 100000000ull, &zero);
             }
         }
+    } else if (warp >= kShipWarp0) {
+        // ======================= partial-S shippers =======================
+        // Once S of tile j is done, lane l of warp 12 + q reads row 32q + l
+        // of it (this CTA's partial scores of the row's 64 keys), releases the
+        // S/P buffer for P, and sends the row's two key halves to the
+        // partner as units 2j and 2j + 1 of its exchange ring, each as soon
+        // as the partner has read the unit its slot held before (three units
+        // back). Dedicated warps make the transfer independent of the
+        // softmax: it starts as soon as S is done and runs while the softmax
+        // of earlier tiles does.
+        const int q = warp - kShipWarp0;
+        const int srow = q * 32 + lane;
+        const uint32_t quad_base = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t r_sx = mapa_shared(sbase + kOffSX, peer);
+        const uint32_t r_sx_full = mapa_shared(bar(BAR_SX_FULL), peer);
+        // the partner's barriers exist before the first remote store
+        cluster_wait();
+        bool ok = true;
+        int sb = 0;
+        uint32_t sph = 0;
+        for (int jj = 0; jj < nrange && ok; ++jj) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_S_FULL + sb), sph, deadline, abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t v[2][32];
+            tmem_ld32(tmem + quad_base + kColSP + sb * 64, v[0]);
+            tmem_ld32(tmem + quad_base + kColSP + sb * 64 + 32, v[1]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_S_READ + sb));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int un = 2 * jj + h, u = un % kSXUnits, use = un / kSXUnits;
+                if (use >= 1 && !__all_sync(0xffffffffu, mbar_wait_cluster(bar(BAR_SX_EMPTY + u), (use - 1) & 1,
+                                                                           deadline, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                // unit layout: [6 stores][128 rows] of 16 bytes (words 4st..4st+3 of a row's 24)
+#pragma unroll
+                for (int st = 0; st < 6; ++st)
+                    st_async_v4(r_sx + u * kSXUnitBytes + (st * kRows + srow) * 16,
+                                make_uint4(pack24_word(v[h], 4 * st), pack24_word(v[h], 4 * st + 1),
+                                           pack24_word(v[h], 4 * st + 2), pack24_word(v[h], 4 * st + 3)),
+                                r_sx_full + 8u * static_cast<uint32_t>(u));
+            }
+            sb = sb == kSPBufs - 1 ? 0 : sb + 1;
+            sph = sb == 0 ? sph ^ 1u : sph;
+        }
+        if (!ok) fail();
+        // this warp's remote stores are over (each lands on the partner's
+        // barrier, which the partner waits for before it leaves)
+        cluster_arrive_release();
     } else {
         // ======================= softmax group (warps 0-7) =======================
         // Warp w serves 16 rows: tensor-memory lanes 32(w%4) + 16(w/4) ..
         // +15 of its lane quadrant. Lanes t and t+16 share a row and take its
         // key halves c = t/16 of every tile, keys [32c, 32c+32), through the
-        // 16x32bx2 access shape. Per tile a thread ships its partial S to the
-        // partner, adds the partner's partial to its own, and runs the
-        // softmax of its row and key half. Both CTAs then hold the same full S
-        // and compute the same P (fp32 addition commutes), each for its own
-        // half of O. The two threads of a row agree on the row max with a
-        // shuffle.
+        // 16x32bx2 access shape. Per tile a thread adds the partner's partial
+        // scores of its row and key half (one unit of the exchange ring) to
+        // its own, both rounded to 24 bits, and runs the softmax of its row
+        // and key half. Both CTAs then hold the same full S and compute the
+        // same P (fp32 addition commutes), each for its own half of O. The two
+        // threads of a row agree on the row max with a shuffle.
         const int quad = warp & 3, sub = warp >> 2, half = lane >> 4;
         const int row = quad * 32 + sub * 16 + (lane & 15);   // TMEM lane of this thread
         const int g = mt * kRows + row;              // row within the sequence
@@ -605,7 +703,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // nodes, and rows of absent nodes come out zero in the end.
         bool node_ok = row_in_seq;
         const int t_tree = (T / kKeys) - t0;  // first tile of the range that can hold node keys
-        const bool lead = row == 0 && half == 0;     // arms each tile's SX byte count
+        const bool lead = row == 0;  // arms the byte count of its key half's units (warp 0, lanes 0 and 16)
         uint64_t m0 = 0, m1 = 0;
         auto resolve_s = [&]() -> bool {
             const bool ready = __all_sync(0xffffffffu, mbar_wait(bar(BAR_TREE), 0, deadline, abort_flag));
@@ -620,12 +718,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // this warp's 16 lanes; the S/P buffer columns of key half 1 start 32
         // columns on, those of O's second half 128 columns on
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32 + sub * 16) << 16;
-        const uint4 *sx = reinterpret_cast<const uint4 *>(smem + kOffSX);   // [16 groups][128 rows] of 4 floats
-        const uint32_t r_sx = mapa_shared(sbase + kOffSX, peer);
-        const uint32_t r_bar_sx_full = mapa_shared(bar(BAR_SX_FULL), peer);
+        const uint4 *sx = reinterpret_cast<const uint4 *>(smem + kOffSX);  // units of [6][128 rows] x 16 B
         const uint32_t r_bar_sx_empty = mapa_shared(bar(BAR_SX_EMPTY), peer);
-        // a row's 64 partial scores are 16 groups of 4; this half's are groups 8c..8c+7
-        const int grp0 = half * 8;
 
         // waits of the softmax group are made warp-uniform, so a lane that
         // gives up can never leave its warp split before a .sync.aligned op
@@ -648,35 +742,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(BAR_QT_READY));
         }
 
-        // this CTA's partial S of a tile (S/P buffer `buf`, barrier phase
-        // parity `par`), this thread's 32 keys
-        auto load_own = [&](int buf, uint32_t par, uint32_t (&sv)[32]) -> bool {
-            if (!wwait(bar(BAR_S_FULL + buf), par)) return false;
-            __syncwarp();
-            tc_fence_after();
-            tmem_ld16x2_32<32>(tmem + lane_base + kColSP + buf * 64, sv);
-            tmem_wait_ld();
-            return true;
-        };
-        auto ship = [&](const uint32_t (&sv)[32]) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                st_async_v4(r_sx + ((grp0 + i) * kRows + row) * 16,
-                            make_uint4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]), r_bar_sx_full);
-        };
 
         // the row sum of this thread's keys, as the sums of its even and odd
         // keys (one packed add per key pair)
         float m_ref = -INFINITY, l_even = 0.f, l_odd = 0.f;
         bool ok = true;
-        // The partial of tile t+1 is loaded and shipped before the softmax of
-        // tile t, so its transfer to the partner overlaps that softmax.
-        uint32_t sv[32];
-        const bool ok0 = load_own(0, 0, sv);
         // the partner's barriers exist before this CTA's first remote operation
         cluster_wait();
-        if (!ok0) ok = false;
-        else ship(sv);
         // tile jj's S/P buffer (jj % kSPBufs) and phase parity ((jj / kSPBufs) & 1),
         // kept as running counters
         int sb = 0;
@@ -685,51 +757,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int nb = sb == kSPBufs - 1 ? 0 : sb + 1;
             const uint32_t nph = sb == kSPBufs - 1 ? sph ^ 1u : sph;
             const int key0 = (t0 + jj) * kKeys + half * 32;
-            // ---- the partner's partial of tile jj: 128 rows x 256 B
-            if (lead) mbar_arrive_expect_tx(bar(BAR_SX_FULL), kSXBytes);
-            if (!wwait_cluster(bar(BAR_SX_FULL), jj & 1)) {
+            // this key half's unit of the partner's partial: unit 2jj + half
+            const int un = 2 * jj + half, u = un % kSXUnits;
+            if (lead) mbar_arrive_expect_tx(bar(BAR_SX_FULL + u), kSXUnitBytes);
+            // this CTA's partial of tile jj (loaded while the partner's is awaited)
+            if (!wwait(bar(BAR_S_FULL + sb), sph)) {
                 ok = false;
                 break;
             }
-            float s[32];
-            // depends on every load from SX (a 128-bit load completes as a
-            // whole, so one word of each is enough)
-            uint32_t read_dep = 0;
+            __syncwarp();
+            tc_fence_after();
+            uint32_t sv[32];
+            tmem_ld16x2_32<32>(tmem + lane_base + kColSP + sb * 64, sv);
+            const bool got = wwait_cluster(bar(BAR_SX_FULL + u), (un / kSXUnits) & 1);
+            tmem_wait_ld();
+            if (!got) {
+                ok = false;
+                break;
+            }
+            // the unit's 24 words of this row; read_dep depends on every load
+            // (a 128-bit load completes as a whole, so one word of each is enough)
+            uint32_t w[24], read_dep = 0;
+            const uint4 *ux = sx + u * (kSXUnitBytes / 16) + row;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint4 o = sx[(grp0 + i) * kRows + row];
+            for (int st = 0; st < 6; ++st) {
+                const uint4 o = ux[st * kRows];
                 read_dep ^= o.x;
-                add_f32x2(__uint_as_float(sv[4 * i]), __uint_as_float(sv[4 * i + 1]), __uint_as_float(o.x),
-                          __uint_as_float(o.y), s[4 * i], s[4 * i + 1]);
-                add_f32x2(__uint_as_float(sv[4 * i + 2]), __uint_as_float(sv[4 * i + 3]), __uint_as_float(o.z),
-                          __uint_as_float(o.w), s[4 * i + 2], s[4 * i + 3]);
+                w[4 * st] = o.x;
+                w[4 * st + 1] = o.y;
+                w[4 * st + 2] = o.z;
+                w[4 * st + 3] = o.w;
             }
-            // hand the buffer back once every read of it is done (the arrive
-            // waits for read_dep); a release would also wait for this
-            // thread's st.async to land in the partner
-            mbar_arrive_remote_relaxed_after(r_bar_sx_empty, read_dep, sBar + NUM_BARS * 8 + 8);
-            // ---- next tile's partial: load it, and ship it once the partner
-            // has read this tile's. The eight stores are spread over the
-            // softmax below: the link to the partner drains at a few tens of
-            // GB/s, and a burst of them would stall this thread until it has.
-            const bool ship_next = jj + 1 < nrange;
-            if (ship_next && (!load_own(nb, nph, sv) || !wwait_cluster(bar(BAR_SX_EMPTY), jj & 1))) {
-                ok = false;
-                break;
+            // hand the slot back once every read of it is done (the arrive
+            // waits for read_dep)
+            mbar_arrive_remote_relaxed_after(r_bar_sx_empty + 8u * static_cast<uint32_t>(u), read_dep,
+                                             sBar + NUM_BARS * 8 + 8);
+            float s[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t pv[4];
+                unpack24(w[3 * c], w[3 * c + 1], w[3 * c + 2], pv);
+                add_f32x2(__uint_as_float(round24(sv[4 * c])), __uint_as_float(round24(sv[4 * c + 1])),
+                          __uint_as_float(pv[0]), __uint_as_float(pv[1]), s[4 * c], s[4 * c + 1]);
+                add_f32x2(__uint_as_float(round24(sv[4 * c + 2])), __uint_as_float(round24(sv[4 * c + 3])),
+                          __uint_as_float(pv[2]), __uint_as_float(pv[3]), s[4 * c + 2], s[4 * c + 3]);
             }
-            auto ship_group = [&](int i) {
-                if (ship_next)
-                    st_async_v4(r_sx + ((grp0 + i) * kRows + row) * 16,
-                                make_uint4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]), r_bar_sx_full);
-            };
-            // The partner needs the next partial before its next tile can
-            // start, so the stores begin at once and are spread over the
-            // softmax: two here, two in the max loop, four in the exp loop.
-            // (Measured on the max-budget workload: eight at once here +12%,
-            // four here and four in the max loop +12%, all eight in the exp
-            // loop +16%, four in each loop 0.8% slower than this split.)
-            ship_group(0);
-            ship_group(1);
             // ---- masked online softmax, log2 domain
             if (!resolved && jj >= t_tree && !resolve_s()) {
                 ok = false;
@@ -750,7 +822,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
             for (int k = 0; k < 32; k += 4) {
-                if ((k & 15) == 0) ship_group(2 + (k >> 4));
                 mxa = fmax3(mxa, s[k], s[k + 1]);
                 mxb = fmax3(mxb, s[k + 2], s[k + 3]);
             }
@@ -769,7 +840,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t pw[32];  // 16 hi words, then 16 lo words
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                if ((k & 3) == 0) ship_group(4 + (k >> 2));
                 float e0, e1, r0, r1;
                 fma_f32x2(s[2 * k], s[2 * k + 1], a.scale_log2, nmref, e0, e1);
                 const float p0 = ex2_approx(e0);
@@ -804,12 +874,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // P is 0 there, but 0 * NaN is NaN: zero those V rows of the tail
             // tile (S, which read them as K, is already complete)
             if (jj >= t_tree && (t0 + jj) * kKeys + kKeys > kend) {  // (jj >= t_tree: the tree is known)
-                uint4 *vset = reinterpret_cast<uint4 *>(smem + kOffRing + (jj % kSlots) * kSlotBytes);
+                uint4 *vset = reinterpret_cast<uint4 *>(smem + kOffRing + (jj % kSlots) * kLatBytes);
                 const int kvalid = kend - (t0 + jj) * kKeys;
 #pragma unroll 1
                 for (int e = half * kRows + row; e < kQChunks * kChunkBytesKV / 16; e += 2 * kRows)
                     if (((e >> 3) & (kKeys - 1)) >= kvalid) vset[e] = make_uint4(0, 0, 0, 0);
                 fence_proxy_async_smem();
+            }
+            // the shippers have read this buffer's S before P overwrites it
+            if (!wwait(bar(BAR_S_READ + sb), sph)) {
+                ok = false;
+                break;
             }
             tmem_st16x2_32<32>(tmem + lane_base + kColSP + sb * 64, pw);
             tmem_wait_st();
@@ -827,9 +902,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) fail();
         __syncwarp();
         tc_fence_after();
-        // This thread's remote operations are over (the last partial shipped,
-        // the last exchange buffer handed back; a release arrival orders them
-        // first): arrive on the cluster barrier that lets the partner leave.
+        // This thread's remote operations are over (the last exchange unit
+        // handed back; a release arrival orders them first): arrive on the
+        // cluster barrier that lets the partner leave.
         // It is waited on only at the very end, so the staging and stores
         // below hold neither CTA. (Arriving right after the tile loop instead
         // measured 0.9% slower on the max-budget workload.)
@@ -868,9 +943,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 (l_sum > 0.f && !zero_row) ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
     }
 
-    // The other threads wait on the setup's cluster barrier now and arrive
-    // on the final one (they made no remote access).
-    if (warp >= kProducerWarp || nrange <= 0) {
+    // The producer, MMA and tree warps wait on the setup's cluster barrier
+    // now and arrive on the final one (they made no remote access).
+    if ((warp >= kProducerWarp && warp < kShipWarp0) || nrange <= 0) {
         cluster_wait();
         cluster_arrive_relaxed();
     }
