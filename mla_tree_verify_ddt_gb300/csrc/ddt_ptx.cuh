@@ -131,6 +131,14 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint4 v, uint3
                  : "memory");
 }
 
+// 4 bytes to the shared memory of another CTA of the cluster, credited to its
+// barrier as above.
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr), "r"(v),
+                 "r"(remote_bar)
+                 : "memory");
+}
+
 // Arrive on a barrier of another CTA without ordering this thread's earlier
 // memory accesses (a relaxed arrival), issued only once `dep` is available:
 // for signals like "I have read your buffer", where a release would also

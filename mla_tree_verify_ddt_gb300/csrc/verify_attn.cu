@@ -83,11 +83,14 @@ constexpr int kSPBufs = 3;          // S / P buffers in tensor memory
 constexpr int kRopeSlots = kSPBufs; // rotary key tiles in flight: the slot of tile j (j % 3) is
                                     // free again once S of tile j - 3 is done
 // The partner's partial S arrives in units of one key half of a tile (128
-// rows x 32 keys), each score the top 24 bits of its float32 pattern, rounded:
-// 12 KB a unit, in a ring of three units (tile j's key half h is unit 2j + h,
-// slot (2j + h) % 3), so a tile's partial can travel while the previous
-// one is still being read.
-constexpr int kSXUnitBytes = kRows * 32 * 3;  // 12288
+// rows x 32 keys) in a ring of three units (tile j's key half h is unit
+// 2j + h, slot (2j + h) % 3), so a tile's partial can travel while the
+// previous one is still being read. A unit row is block-scaled: 32 16-bit
+// integers q (offset by 32768) and the scale d, the score being q d (see
+// quantize_unit); the 16-byte groups of the 128 rows come first, then the
+// rows' scales.
+constexpr int kSXMantBytes = kRows * 64;                  // 8192
+constexpr int kSXUnitBytes = kSXMantBytes + kRows * 4;    // 8704
 constexpr int kSXUnits = 3;
 
 // shared memory map (offsets from a 1024-aligned base)
@@ -135,7 +138,7 @@ enum {
     BAR_DRAIN = 20,      // the S issuer's MMAs, after a failure
     BAR_TREE = 21,       // the tree's node count and this tile's node masks are in shared memory
     BAR_DRAIN_PV = 22,   // the PV issuer's MMAs, after a failure
-    BAR_S_READ = 23,     // kSPBufs: the shippers have read S of the buffer (P may overwrite it)
+    BAR_S_READ = 23,     // kSPBufs: the shippers have sent S of the buffer and left its block-scaled values
     // exchange ring, one barrier per unit slot
     BAR_SX_FULL = 26,    // kSXUnits: the partner's unit is in my slot (its bytes come from the partner)
     BAR_SX_EMPTY = 29,   // kSXUnits: the partner has read the unit my shippers wrote into its slot
@@ -243,28 +246,51 @@ __device__ __noinline__ void stage_chunk(uint32_t o_col, uint8_t *ring, int half
     }
 }
 
-// Partial scores cross the cluster as the top 24 bits of their float32
-// patterns, rounded to nearest (adding 0x80 carries a low byte of 0x80 or more
-// into them): four scores in three words. Word k of a run of rounded patterns
-// r[0..]: bytes 1-3 of r[4g], then of r[4g+1], ... packed low byte first.
-__device__ __forceinline__ uint32_t pack24_word(const uint32_t *r, int k) {
-    const int g = 4 * (k / 3);
-    switch (k % 3) {
-        case 0: return __byte_perm(r[g] + 0x80u, r[g + 1] + 0x80u, 0x5321);
-        case 1: return __byte_perm(r[g + 1] + 0x80u, r[g + 2] + 0x80u, 0x6532);
-        default: return __byte_perm(r[g + 2] + 0x80u, r[g + 3] + 0x80u, 0x7653);
+// Partial scores cross the cluster block-scaled: the 32 scores x_k of a row
+// and key half with m = max |x_k| become q_k = round(x_k 32767 / m), integers
+// in [-32767, 32767], sent as q_k + 32768 in 16 bits, and the scale
+// d = m / 32767; the score used is q_k d (float32 products). The CTA that
+// owns the scores uses the same q_k d in place of its own, so both CTAs add
+// the same two terms. |x_k - q_k d| <= m / 65534 (plus float32 rounding), and
+// the keys that decide a softmax have the largest scores, for which that is
+// the float32 value rounded to about 16 significant bits. (The scale factor
+// 32767 / m may be approximate: |x_k| 32767 / m stays below 32767.5, and the
+// products use d alone.) q_k + 32768 is the low 16 bits of the float32
+// x_k (32767 / m) + 2^23 + 2^15, a number in [2^23, 2^24) rounded to an
+// integer by the fused multiply-add, whose high 16 bits are 0x4B00; the
+// receiver rebuilds that float from the 16 bits and subtracts 2^23 + 2^15
+// exactly.
+constexpr float kQBias = 8421376.0f;  // 2^23 + 2^15
+
+// The 32 partial scores x (float32 patterns) of a row and key half: their
+// packed 16-bit codes (value 2p in the low half of word p), their scale, and
+// in x the values q d that stand for them.
+__device__ __forceinline__ float quantize_unit(uint32_t (&x)[32], uint32_t (&code)[16]) {
+    float m = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) m = fmaxf(m, fabsf(__uint_as_float(x[k])));
+    const float c = m > 1e-30f ? __fdividef(32767.0f, m) : 0.f;
+    const float d = m * (1.0f / 32767.0f);
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+        float y0, y1, q0, q1, v0, v1;
+        fma_f32x2(__uint_as_float(x[2 * p]), __uint_as_float(x[2 * p + 1]), c, kQBias, y0, y1);
+        code[p] = __byte_perm(__float_as_uint(y0), __float_as_uint(y1), 0x5410);
+        sub_f32x2(y0, y1, kQBias, kQBias, q0, q1);
+        mul_f32x2(q0, q1, d, d, v0, v1);
+        x[2 * p] = __float_as_uint(v0);
+        x[2 * p + 1] = __float_as_uint(v1);
     }
+    return d;
 }
-// The four rounded float32 patterns (low byte zero) packed in w0, w1, w2.
-__device__ __forceinline__ void unpack24(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t (&v)[4]) {
-    v[0] = __byte_perm(w0, 0u, 0x2104);
-    v[1] = __byte_perm(w0, w1, 0x5430) & 0xFFFFFF00u;
-    v[2] = __byte_perm(w1, w2, 0x4320) & 0xFFFFFF00u;
-    v[3] = w2 & 0xFFFFFF00u;
+
+// The two values q d of code word w (scale d).
+__device__ __forceinline__ void dequantize_pair(uint32_t w, float d, float &v0, float &v1) {
+    float q0, q1;
+    sub_f32x2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7610)), __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7632)),
+              kQBias, kQBias, q0, q1);
+    mul_f32x2(q0, q1, d, d, v0, v1);
 }
-// The same rounding of a pattern the CTA keeps (its own partial), so both
-// CTAs add the same two rounded terms.
-__device__ __forceinline__ uint32_t round24(uint32_t x) { return (x + 0x80u) & 0xFFFFFF00u; }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
@@ -629,16 +655,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp >= kShipWarp0) {
         // ======================= partial-S shippers =======================
         // Once S of tile j is done, lane l of warp 12 + q reads row 32q + l
-        // of it (this CTA's partial scores of the row's 64 keys), releases the
-        // S/P buffer for P, and sends the row's two key halves to the
-        // partner as units 2j and 2j + 1 of its exchange ring, each as soon
-        // as the partner has read the unit its slot held before (three units
-        // back). Dedicated warps make the transfer independent of the
+        // of it (this CTA's partial scores of the row's 64 keys), block-scales
+        // each key half and sends it to the partner as unit 2j + h of its
+        // exchange ring, as soon as the partner has read the unit its slot
+        // held before (three units back); then it writes the scaled values
+        // back in place of its own scores and releases the buffer to the
+        // softmax. Dedicated warps make the transfer independent of the
         // softmax: it starts as soon as S is done and runs while the softmax
         // of earlier tiles does.
         const int q = warp - kShipWarp0;
         const int srow = q * 32 + lane;
         const uint32_t quad_base = static_cast<uint32_t>(q * 32) << 16;
+        const int t_tree = (T / kKeys) - t0;  // first tile of the range that can hold node keys
         const uint32_t r_sx = mapa_shared(sbase + kOffSX, peer);
         const uint32_t r_sx_full = mapa_shared(bar(BAR_SX_FULL), peer);
         // the partner's barriers exist before the first remote store
@@ -656,25 +684,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld32(tmem + quad_base + kColSP + sb * 64, v[0]);
             tmem_ld32(tmem + quad_base + kColSP + sb * 64 + 32, v[1]);
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_S_READ + sb));
+            // KV rows past the sequence's key end may hold anything: their
+            // scores are set to 0 so they cannot widen a unit's scale (the
+            // softmax hides those keys). Only tiles that reach past the prefix
+            // can hold such keys; the key end is known once the tree is.
+            if (jj >= t_tree) {
+                if (!resolved) {
+                    const bool ready = __all_sync(0xffffffffu, mbar_wait(bar(BAR_TREE), 0, deadline, abort_flag));
+                    resolve(ready, ready ? *tree_n : 0);
+                    if (!ready) {
+                        ok = false;
+                        break;
+                    }
+                }
+                const int kbase = (t0 + jj) * kKeys;
+#pragma unroll
+                for (int k = 0; k < kKeys; ++k)
+                    if (kbase + k >= kend) v[k >> 5][k & 31] = 0u;
+            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+                uint32_t code[16];
+                const float dsc = quantize_unit(v[h], code);
                 const int un = 2 * jj + h, u = un % kSXUnits, use = un / kSXUnits;
                 if (use >= 1 && !__all_sync(0xffffffffu, mbar_wait_cluster(bar(BAR_SX_EMPTY + u), (use - 1) & 1,
                                                                            deadline, abort_flag))) {
                     ok = false;
                     break;
                 }
-                // unit layout: [6 stores][128 rows] of 16 bytes (words 4st..4st+3 of a row's 24)
+                // unit layout: [4 stores][128 rows] of 16 bytes (code words 4st..4st+3), then the scales
+                const uint32_t dst = r_sx + u * kSXUnitBytes, ubar = r_sx_full + 8u * static_cast<uint32_t>(u);
 #pragma unroll
-                for (int st = 0; st < 6; ++st)
-                    st_async_v4(r_sx + u * kSXUnitBytes + (st * kRows + srow) * 16,
-                                make_uint4(pack24_word(v[h], 4 * st), pack24_word(v[h], 4 * st + 1),
-                                           pack24_word(v[h], 4 * st + 2), pack24_word(v[h], 4 * st + 3)),
-                                r_sx_full + 8u * static_cast<uint32_t>(u));
+                for (int st = 0; st < 4; ++st)
+                    st_async_v4(dst + (st * kRows + srow) * 16,
+                                make_uint4(code[4 * st], code[4 * st + 1], code[4 * st + 2], code[4 * st + 3]), ubar);
+                st_async_b32(dst + kSXMantBytes + srow * 4, __float_as_uint(dsc), ubar);
+                // the values both CTAs use for this key half of this CTA's partial, in place of it
+                tmem_st32(tmem + quad_base + kColSP + sb * 64 + 32 * h, v[h]);
             }
+            if (!ok) break;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_S_READ + sb));
             sb = sb == kSPBufs - 1 ? 0 : sb + 1;
             sph = sb == 0 ? sph ^ 1u : sph;
         }
@@ -689,8 +741,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // key halves c = t/16 of every tile, keys [32c, 32c+32), through the
         // 16x32bx2 access shape. Per tile a thread adds the partner's partial
         // scores of its row and key half (one unit of the exchange ring) to
-        // its own, both rounded to 24 bits, and runs the softmax of its row
-        // and key half. Both CTAs then hold the same full S and compute the
+        // its own, both block-scaled, and runs the softmax of its row and key
+        // half. Both CTAs then hold the same full S and compute the
         // same P (fp32 addition commutes), each for its own half of O. The two
         // threads of a row agree on the row max with a shuffle.
         const int quad = warp & 3, sub = warp >> 2, half = lane >> 4;
@@ -760,8 +812,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // this key half's unit of the partner's partial: unit 2jj + half
             const int un = 2 * jj + half, u = un % kSXUnits;
             if (lead) mbar_arrive_expect_tx(bar(BAR_SX_FULL + u), kSXUnitBytes);
-            // this CTA's partial of tile jj (loaded while the partner's is awaited)
-            if (!wwait(bar(BAR_S_FULL + sb), sph)) {
+            // this CTA's partial of tile jj as the shippers left it, block-scaled
+            // (loaded while the partner's is awaited)
+            if (!wwait(bar(BAR_S_READ + sb), sph)) {
                 ok = false;
                 break;
             }
@@ -775,12 +828,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            // the unit's 24 words of this row; read_dep depends on every load
-            // (a 128-bit load completes as a whole, so one word of each is enough)
-            uint32_t w[24], read_dep = 0;
+            // the unit's 16 code words and scale of this row; read_dep depends
+            // on every load (a 128-bit load completes as a whole, so one word
+            // of each is enough)
+            uint32_t w[16];
             const uint4 *ux = sx + u * (kSXUnitBytes / 16) + row;
+            const uint32_t dbits = reinterpret_cast<const uint32_t *>(smem + kOffSX + u * kSXUnitBytes + kSXMantBytes)[row];
+            uint32_t read_dep = dbits;
 #pragma unroll
-            for (int st = 0; st < 6; ++st) {
+            for (int st = 0; st < 4; ++st) {
                 const uint4 o = ux[st * kRows];
                 read_dep ^= o.x;
                 w[4 * st] = o.x;
@@ -794,13 +850,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                              sBar + NUM_BARS * 8 + 8);
             float s[32];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t pv[4];
-                unpack24(w[3 * c], w[3 * c + 1], w[3 * c + 2], pv);
-                add_f32x2(__uint_as_float(round24(sv[4 * c])), __uint_as_float(round24(sv[4 * c + 1])),
-                          __uint_as_float(pv[0]), __uint_as_float(pv[1]), s[4 * c], s[4 * c + 1]);
-                add_f32x2(__uint_as_float(round24(sv[4 * c + 2])), __uint_as_float(round24(sv[4 * c + 3])),
-                          __uint_as_float(pv[2]), __uint_as_float(pv[3]), s[4 * c + 2], s[4 * c + 3]);
+            for (int p = 0; p < 16; ++p) {
+                float v0, v1;
+                dequantize_pair(w[p], __uint_as_float(dbits), v0, v1);
+                add_f32x2(__uint_as_float(sv[2 * p]), __uint_as_float(sv[2 * p + 1]), v0, v1, s[2 * p], s[2 * p + 1]);
             }
             // ---- masked online softmax, log2 domain
             if (!resolved && jj >= t_tree && !resolve_s()) {
@@ -880,11 +933,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int e = half * kRows + row; e < kQChunks * kChunkBytesKV / 16; e += 2 * kRows)
                     if (((e >> 3) & (kKeys - 1)) >= kvalid) vset[e] = make_uint4(0, 0, 0, 0);
                 fence_proxy_async_smem();
-            }
-            // the shippers have read this buffer's S before P overwrites it
-            if (!wwait(bar(BAR_S_READ + sb), sph)) {
-                ok = false;
-                break;
             }
             tmem_st16x2_32<32>(tmem + lane_base + kColSP + sb * 64, pw);
             tmem_wait_st();
