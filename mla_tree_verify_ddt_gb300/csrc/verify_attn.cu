@@ -263,25 +263,26 @@ __device__ __noinline__ void stage_chunk(uint32_t o_col, uint8_t *ring, int half
 constexpr float kQBias = 8421376.0f;  // 2^23 + 2^15
 
 // The 32 partial scores x (float32 patterns) of a row and key half: their
-// packed 16-bit codes (value 2p in the low half of word p), their scale, and
-// in x the values q d that stand for them.
-__device__ __forceinline__ float quantize_unit(uint32_t (&x)[32], uint32_t (&code)[16]) {
-    float m = 0.f;
+// packed 16-bit codes (value 2p in the low half of word p) and their scale.
+// The maximum is taken as a tree (a chain of 32 dependent maxima would cost
+// its full latency).
+__device__ __forceinline__ float quantize_unit(const uint32_t (&x)[32], uint32_t (&code)[16]) {
+    float a[16];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) m = fmaxf(m, fabsf(__uint_as_float(x[k])));
+    for (int k = 0; k < 16; ++k) a[k] = fmaxf(fabsf(__uint_as_float(x[2 * k])), fabsf(__uint_as_float(x[2 * k + 1])));
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w; ++k) a[k] = fmaxf(a[k], a[k + w]);
+    const float m = a[0];
     const float c = m > 1e-30f ? __fdividef(32767.0f, m) : 0.f;
-    const float d = m * (1.0f / 32767.0f);
 #pragma unroll
     for (int p = 0; p < 16; ++p) {
-        float y0, y1, q0, q1, v0, v1;
+        float y0, y1;
         fma_f32x2(__uint_as_float(x[2 * p]), __uint_as_float(x[2 * p + 1]), c, kQBias, y0, y1);
         code[p] = __byte_perm(__float_as_uint(y0), __float_as_uint(y1), 0x5410);
-        sub_f32x2(y0, y1, kQBias, kQBias, q0, q1);
-        mul_f32x2(q0, q1, d, d, v0, v1);
-        x[2 * p] = __float_as_uint(v0);
-        x[2 * p + 1] = __float_as_uint(v1);
     }
-    return d;
+    return m * (1.0f / 32767.0f);
 }
 
 // The two values q d of code word w (scale d).
@@ -720,6 +721,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 make_uint4(code[4 * st], code[4 * st + 1], code[4 * st + 2], code[4 * st + 3]), ubar);
                 st_async_b32(dst + kSXMantBytes + srow * 4, __float_as_uint(dsc), ubar);
                 // the values both CTAs use for this key half of this CTA's partial, in place of it
+#pragma unroll
+                for (int p = 0; p < 16; ++p) {
+                    float v0, v1;
+                    dequantize_pair(code[p], dsc, v0, v1);
+                    v[h][2 * p] = __float_as_uint(v0);
+                    v[h][2 * p + 1] = __float_as_uint(v1);
+                }
                 tmem_st32(tmem + quad_base + kColSP + sb * 64 + 32 * h, v[h]);
             }
             if (!ok) break;
