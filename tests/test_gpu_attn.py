@@ -3,6 +3,7 @@
 Small cases are compared on every row; the large workloads, in the launch
 configuration the benchmark times, on sampled rows the oracle computes one
 by one. Tolerance: max-abs 2e-3 and rel 1e-2 per element (gpu_util)."""
+import dataclasses
 import math
 
 import numpy as np
@@ -139,6 +140,23 @@ def test_full_parity_ragged_prefixes_over_row_tiles(seed, B, T):
     ws = ddtree.ddt_workspace_size(B, wl.D, wl.K, wl.budget, wl.H, inp.Tcap)
     assert ws > 0, "the key range must be split"
     full_check(inp, f"ragged prefixes, seed {seed}")
+
+
+@pytest.mark.parametrize("case", ["custom1", "custom2", "single_stream"])
+def test_full_parity_sharp_logits(case):
+    """Logits eight times sharper than the N(0,1) inputs give (the softmax
+    scale multiplied by 8): the partner's partial scores cross the cluster
+    block-scaled to 16 bits, an error in proportion to the scores' magnitude,
+    and the output must still meet the tolerance on every row."""
+    if case == "single_stream":
+        inp = synth.make_inputs(1)
+    elif case == "custom1":
+        inp = custom_inputs(1, 3, 5, 4, 20, 8, [0, 37, 300])
+    else:
+        inp = custom_inputs(2, 2, 16, 8, 64, 2, [129, 64])
+    inp = dataclasses.replace(inp, scale=inp.scale * 8.0)
+    err = full_check(inp, f"{case}, logits x8")
+    print(f"max abs err {err:.3e}")
 
 
 @pytest.mark.parametrize("idx", [2, 3, 4])
