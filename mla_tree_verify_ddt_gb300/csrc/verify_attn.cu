@@ -24,18 +24,20 @@
 //    the V of its half of the output, so O += P V (M=128, N=256, K=64) needs
 //    no further load. Nothing is loaded or multiplied twice and each CTA
 //    keeps only part of Q and half of each KV row (36 KB per 64-key tile) in
-//    shared memory, which leaves room for four KV tiles in flight.
+//    shared memory: four latent tiles in flight, and three of the small
+//    rotary parts (free as soon as their S is done).
 //  * Tensor memory: O (256 columns), three S/P buffers of 64 columns, and the
 //    query's fourth latent chunk plus its rotary part as MMA A operands (the
 //    other three latent chunks are in shared memory). Each thread overwrites
 //    its own lane of S with the P of that tile once it has read S, so S and
 //    P share buffers and a buffer is reused three tiles later, after its PV.
-//  * Each softmax thread ships its 32 keys of the CTA's partial S to the
-//    partner with st.async (bytes credited to the partner's mbarrier on
-//    arrival), spread over the softmax of the previous tile, and adds the
-//    partner's partial to its own. Both CTAs then hold the same full S and
-//    run the same softmax, each for its own half of O: no probabilities
-//    cross the cluster.
+//  * Four shipper warps send each tile's partial S to the partner as soon as
+//    it is done, block-scaled to 16 bits per score, with st.async (bytes
+//    credited to the partner's mbarrier on arrival) into a ring of three
+//    half-tile units, and leave the same scaled values in place of their own
+//    partial. Each softmax thread adds the partner's unit to its own. Both
+//    CTAs then hold the same full S and run the same softmax, each for its
+//    own half of O: no probabilities cross the cluster.
 //  * Softmax in fp32, log2 domain, two threads per row: lanes t and t+16 of
 //    one warp read the same tensor-memory lane (the 16x32bx2 access shape),
 //    32 keys each, and combine their tile max and, at the end, their row sums
@@ -98,8 +100,8 @@ constexpr int kOffQ = 0;
 constexpr int kOffRing = kOffQ + kQSmemChunks * kChunkBytesQ;     // 49152: latent ring
 constexpr int kOffRope = kOffRing + kSlots * kLatBytes;           // 180224: rotary ring
 constexpr int kOffSX = kOffRope + kRopeSlots * kKRopeBytes;       // 192512: exchange ring
-constexpr int kOffBar = kOffSX + kSXUnits * kSXUnitBytes;         // 229376: barriers and flags (272 B)
-constexpr int kOffTree = kOffBar + 272;                           // 229648: the tree as this CTA needs it
+constexpr int kOffBar = kOffSX + kSXUnits * kSXUnitBytes;         // 218624: barriers and flags (272 B)
+constexpr int kOffTree = kOffBar + 272;                           // 218896: the tree as this CTA needs it
 constexpr int kMaxTileNodes = DDT_MAX_BUDGET + 1;                 // nodes a 128-row tile can span (<= Qc)
 constexpr int kTreeBytes = 16 + kMaxTileNodes * 16;               // node count, then 2 mask words per node
 constexpr int kSmemBytes = kOffTree + kTreeBytes + 1024;          // + alignment slack
@@ -778,7 +780,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // this warp's 16 lanes; the S/P buffer columns of key half 1 start 32
         // columns on, those of O's second half 128 columns on
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32 + sub * 16) << 16;
-        const uint4 *sx = reinterpret_cast<const uint4 *>(smem + kOffSX);  // units of [6][128 rows] x 16 B
+        const uint4 *sx = reinterpret_cast<const uint4 *>(smem + kOffSX);  // units: [4][128 rows] x 16 B, then scales
         const uint32_t r_bar_sx_empty = mapa_shared(bar(BAR_SX_EMPTY), peer);
 
         // waits of the softmax group are made warp-uniform, so a lane that
