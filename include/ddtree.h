@@ -45,7 +45,10 @@
  *    found in the DATA are reported per sequence in tree->status on the device
  *    without any sync: DDT_E_BADINPUT (bad drafter row, token out of range,
  *    prefix length out of range) or DDT_E_TIMEOUT (a bounded on-chip wait
- *    expired). A flagged sequence still gets defined outputs: a root-only tree
+ *    expired); the attention kernel writes DDT_E_CUDA to every sequence
+ *    if it finds its shared memory misaligned for its operand
+ *    layouts (not expected; its outputs are then undefined). A flagged
+ *    sequence otherwise still gets defined outputs: a root-only tree
  *    (n_nodes = 1), zero attention rows, accept_len = 1.
  */
 #ifndef DDTREE_H
@@ -100,7 +103,7 @@ typedef struct ddt_tree {
     int32_t *next_sibling;   /* [B,Qc] next larger index with the same parent or -1 */
     uint64_t *mask;          /* [B,Qc,W] bit m of node i: m is i or an ancestor of i */
     int32_t *n_nodes;        /* [B] 1 + selected draft nodes */
-    int32_t *status;         /* [B] DDT_OK / DDT_E_BADINPUT / DDT_E_TIMEOUT */
+    int32_t *status;         /* [B] DDT_OK / DDT_E_BADINPUT / DDT_E_TIMEOUT (/ DDT_E_CUDA, see above) */
 } ddt_tree;
 
 /* Attention inputs in bfloat16 (raw 16-bit patterns). Node m of sequence b

@@ -24,16 +24,15 @@
 //    the V of its half of the output, so O += P V (M=128, N=256, K=64) needs
 //    no further load. Nothing is loaded or multiplied twice and each CTA
 //    keeps only part of Q and half of each KV row (36 KB per 64-key tile) in
-//    shared memory: four latent tiles in flight, and three of the small
+//    shared memory: four latent tiles in flight, and two of the small
 //    rotary parts (free as soon as their S is done).
-//  * Tensor memory: O (256 columns), three S/P buffers of 64 columns, and the
-//    query's fourth latent chunk plus its rotary part as MMA A operands (the
-//    other three latent chunks are in shared memory). Each thread overwrites
-//    its own lane of S with the P of that tile once it has read S, so S and
-//    P share buffers and a buffer is reused three tiles later, after its PV.
+//  * Tensor memory: O (256 columns) and four S/P buffers of 64 columns; the
+//    query is in shared memory. Each thread overwrites its own lane of S with
+//    the P of that tile once it has read S, so S and P share buffers and a
+//    buffer is reused four tiles later, after its PV.
 //  * Four shipper warps send each tile's partial S to the partner as soon as
 //    it is done, block-scaled to 16 bits per score, with st.async (bytes
-//    credited to the partner's mbarrier on arrival) into a ring of three
+//    credited to the partner's mbarrier on arrival) into a ring of two
 //    half-tile units, and leave the same scaled values in place of their own
 //    partial. Each softmax thread adds the partner's unit to its own. Both
 //    CTAs then hold the same full S and run the same softmax, each for its
@@ -73,49 +72,50 @@ namespace {
 constexpr int kRows = 128;          // rows per cluster (MMA M)
 constexpr int kKeys = 64;           // keys per tile (S MMA N)
 constexpr int kQChunks = 4;         // latent query/KV chunks per CTA: 4 x 64 columns
-constexpr int kQSmemChunks = 3;     // query chunks 0-2 in shared memory; chunk 3 and the
-                                    // rotary columns sit in tensor memory (A operands)
+constexpr int kQSmemChunks = 4;     // the query's latent chunks, in shared memory
 constexpr int kChunkBytesQ = kRows * 128;    // 64 bf16 x 128 rows, 128-byte swizzle
 constexpr int kChunkBytesKV = kKeys * 128;   // 64 bf16 x 64 keys
 constexpr int kKRopeBytes = kKeys * 64;      // 32 bf16 x 64 keys, 64-byte swizzle
+constexpr int kQRopeBytes = kRows * 64;      // 32 bf16 x 128 rows, 64-byte swizzle
 constexpr int kLatBytes = kQChunks * kChunkBytesKV;  // 32768: a tile's latent keys (and its V)
 constexpr int kTileBytes = kLatBytes + kKRopeBytes;  // 36864: a tile's bytes in shared memory
 constexpr int kSlots = 4;           // latent KV tiles in flight
-constexpr int kSPBufs = 3;          // S / P buffers in tensor memory
-constexpr int kRopeSlots = kSPBufs; // rotary key tiles in flight: the slot of tile j (j % 3) is
-                                    // free again once S of tile j - 3 is done
+constexpr int kSPBufs = 4;          // S / P buffers in tensor memory
+constexpr int kRopeSlots = 2;       // rotary key tiles in flight: the slot of tile j (j % 2) is
+                                    // free again once S of tile j - 2 is done
 // The partner's partial S arrives in units of one key half of a tile (128
-// rows x 32 keys) in a ring of three units (tile j's key half h is unit
-// 2j + h, slot (2j + h) % 3), so a tile's partial can travel while the
-// previous one is still being read. A unit row is block-scaled: 32 16-bit
+// rows x 32 keys) in a ring of two units (tile j's key half h is unit
+// 2j + h, slot h). A unit row is block-scaled: 32 16-bit
 // integers q (offset by 32768) and the scale d, the score being q d (see
 // quantize_unit); the 16-byte groups of the 128 rows come first, then the
 // rows' scales.
 constexpr int kSXMantBytes = kRows * 64;                  // 8192
 constexpr int kSXUnitBytes = kSXMantBytes + kRows * 4;    // 8704
-constexpr int kSXUnits = 3;
+constexpr int kSXUnits = 2;
 
-// shared memory map (offsets from a 1024-aligned base)
+// shared memory map (offsets from the dynamic shared memory base, which is
+// 1024-aligned: checked at run time)
 constexpr int kOffQ = 0;
-constexpr int kOffRing = kOffQ + kQSmemChunks * kChunkBytesQ;     // 49152: latent ring
-constexpr int kOffRope = kOffRing + kSlots * kLatBytes;           // 180224: rotary ring
-constexpr int kOffSX = kOffRope + kRopeSlots * kKRopeBytes;       // 192512: exchange ring
-constexpr int kOffBar = kOffSX + kSXUnits * kSXUnitBytes;         // 218624: barriers and flags (272 B)
-constexpr int kOffTree = kOffBar + 272;                           // 218896: the tree as this CTA needs it
+constexpr int kOffQR = kOffQ + kQSmemChunks * kChunkBytesQ;       // 65536: rotary query
+constexpr int kOffRing = kOffQR + kQRopeBytes;                    // 73728: latent ring
+constexpr int kOffRope = kOffRing + kSlots * kLatBytes;           // 204800: rotary ring
+constexpr int kOffSX = kOffRope + kRopeSlots * kKRopeBytes;       // 212992: exchange ring
+constexpr int kOffBar = kOffSX + kSXUnits * kSXUnitBytes;         // 230400: barriers and flags (288 B)
+constexpr int kOffTree = kOffBar + 288;                           // 230688: the tree as this CTA needs it
 constexpr int kMaxTileNodes = DDT_MAX_BUDGET + 1;                 // nodes a 128-row tile can span (<= Qc)
 constexpr int kTreeBytes = 16 + kMaxTileNodes * 16;               // node count, then 2 mask words per node
-constexpr int kSmemBytes = kOffTree + kTreeBytes + 1024;          // + alignment slack
+constexpr int kSmemBytes = kOffTree + kTreeBytes;
+static_assert(kOffRing % 1024 == 0 && kOffQR % 1024 == 0 && kOffRope % 512 == 0, "swizzle atom alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 constexpr int kOutBoxBytes = kRows * 128;                         // output staging: 128 rows x 32 fp32
 static_assert(8 * kOutBoxBytes <= kSlots * kLatBytes, "output staging must fit in the latent ring");
 
 // tensor memory columns
 constexpr uint32_t kColO = 0;       // 256: this CTA's half of O
-constexpr uint32_t kColSP = 256;    // 3 x 64: partial S of a tile, overwritten in place (lane by
+constexpr uint32_t kColSP = 256;    // 4 x 64: partial S of a tile, overwritten in place (lane by
                                     // lane, once read) by its P: 32 hi words then 32 lo words
-constexpr uint32_t kColQ3 = 448;    // 32: latent query chunk 3 (bf16 pairs)
-constexpr uint32_t kColQR = 480;    // 16: rotary query (bf16 pairs)
 constexpr uint32_t kTmemCols = 512;
+static_assert(kColSP + kSPBufs * 64 <= kTmemCols, "tensor memory");
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // warps 0-7 softmax group (two threads per row), 8 TMA producer, 9 S-MMA
@@ -129,30 +129,30 @@ constexpr int kThreads = 512;
 constexpr int kProducerWarp = 8, kMmaWarp = 9, kTreeWarp = 10, kPvWarp = 11, kShipWarp0 = 12;
 
 enum {
-    BAR_Q_FULL = 0,
-    BAR_QT_READY = 1,    // query chunk 3 and rotary query written to tensor memory
-    BAR_RING_FULL = 2,   // kSlots
-    BAR_RING_EMPTY = 6,  // kSlots
-    BAR_S_FULL = 10,     // kSPBufs
+    BAR_Q_FULL = 0,      // the query (latent chunks and rotary part) is in shared memory
+    BAR_RING_FULL = 1,   // kSlots
+    BAR_RING_EMPTY = 5,  // kSlots
+    BAR_S_FULL = 9,      // kSPBufs
     BAR_P_FULL = 13,     // kSPBufs
-    BAR_PV_DONE = 16,    // kSPBufs
-    BAR_O_FINAL = 19,
-    BAR_DRAIN = 20,      // the S issuer's MMAs, after a failure
-    BAR_TREE = 21,       // the tree's node count and this tile's node masks are in shared memory
-    BAR_DRAIN_PV = 22,   // the PV issuer's MMAs, after a failure
-    BAR_S_READ = 23,     // kSPBufs: the shippers have sent S of the buffer and left its block-scaled values
+    BAR_PV_DONE = 17,    // kSPBufs
+    BAR_O_FINAL = 21,
+    BAR_DRAIN = 22,      // the S issuer's MMAs, after a failure
+    BAR_TREE = 23,       // the tree's node count and this tile's node masks are in shared memory
+    BAR_DRAIN_PV = 24,   // the PV issuer's MMAs, after a failure
+    BAR_S_READ = 25,     // kSPBufs: the shippers have sent S of the buffer and left its block-scaled values
     // exchange ring, one barrier per unit slot
-    BAR_SX_FULL = 26,    // kSXUnits: the partner's unit is in my slot (its bytes come from the partner)
-    BAR_SX_EMPTY = 29,   // kSXUnits: the partner has read the unit my shippers wrote into its slot
-    NUM_BARS = 32        // (one per lane of the initialising warp)
+    BAR_SX_FULL = 29,    // kSXUnits: the partner's unit is in my slot (its bytes come from the partner)
+    BAR_SX_EMPTY = 31,   // kSXUnits: the partner has read the unit my shippers wrote into its slot
+    NUM_BARS = 33
 };
-static_assert(kRopeSlots == kSPBufs, "a rotary slot is released by the S_FULL barrier of the same index");
+static_assert(NUM_BARS * 8 + 12 <= kOffTree - kOffBar, "barrier region");
+static_assert(BAR_SX_EMPTY + kSXUnits == NUM_BARS, "barrier numbering");
 
 // arrival count of barrier i (see the enum); with a block-table cache the
 // ring is filled by the 64 lanes of two gather warps instead of TMA
 __device__ __forceinline__ uint32_t bar_count(int i, bool gathered) {
     if (gathered && i >= BAR_RING_FULL && i < BAR_RING_FULL + kSlots) return 64;  // two gather warps
-    if (i == BAR_QT_READY || (i >= BAR_P_FULL && i < BAR_P_FULL + kSPBufs)) return 8;  // one per softmax warp
+    if (i >= BAR_P_FULL && i < BAR_P_FULL + kSPBufs) return 8;                            // one per softmax warp
     if (i >= BAR_S_READ && i < BAR_S_READ + kSPBufs) return 4;                          // one per shipper warp
     if (i >= BAR_SX_EMPTY && i < BAR_SX_EMPTY + kSXUnits) return kRows;  // the partner's threads of one key half
     return 1;  // one arrival (SX_FULL: the arming thread; its bytes come from the partner's st.async)
@@ -163,8 +163,6 @@ struct AttnArgs {
     const uint64_t *mask;
     const int32_t *n_nodes;
     const int32_t *prefix_len;
-    const uint16_t *q_lat;   // for query chunk 3, loaded straight into tensor memory
-    const uint16_t *q_rope;
     int32_t *status;
     float *o_dst;            // [nsplit][rows_total][512] (nsplit == 1: the final output)
     float *lse_dst;          // [nsplit][rows_total]
@@ -296,10 +294,10 @@ __device__ __forceinline__ void dequantize_pair(uint32_t w, float d, float &v0, 
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    verify_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                       const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_o,
-                       const AttnArgs a) {
-    extern __shared__ uint8_t smem_raw[];
+    verify_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
+                       const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kr,
+                       const __grid_constant__ CUtensorMap tm_o, const AttnArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.x >> 1;
@@ -312,36 +310,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // are issued here and first used after the barrier / tensor-memory /
     // cluster setup below, which hides their latency.
     const int T_in = a.prefix_len[b];
-    // Each softmax thread's part of its row's query that tensor memory holds
-    // (latent chunk 3 for key-half-0 warps, the rotary query for key-half-1
-    // warps), loaded here for the same reason.
-    uint32_t q_pre[32];
-#pragma unroll
-    for (int v = 0; v < 32; ++v) q_pre[v] = 0;
-    if (warp < 8) {
-        const int g_pre = mt * kRows + (warp & 3) * 32 + lane;
-        if (g_pre < a.Qc * a.H) {
-            const size_t r_pre = static_cast<size_t>(b) * a.Qc * a.H + g_pre;
-            const uint4 *src = (warp >> 2) == 0
-                                   ? reinterpret_cast<const uint4 *>(a.q_lat + r_pre * 512 + rank * 256 + 192)
-                                   : reinterpret_cast<const uint4 *>(a.q_rope + r_pre * 64 + rank * 32);
-            const int nv = (warp >> 2) == 0 ? 8 : 4;
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                if (v < nv) {
-                    const uint4 x = src[v];
-                    q_pre[4 * v] = x.x;
-                    q_pre[4 * v + 1] = x.y;
-                    q_pre[4 * v + 2] = x.z;
-                    q_pre[4 * v + 3] = x.w;
-                }
-            }
-        }
-    }
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + kOffQ, sRing = sbase + kOffRing, sRope = sbase + kOffRope;
+    // The swizzled operand layouts need a 1024-aligned base, which the
+    // declaration asks for; shared memory has no room to align it here.
+    if (sbase & 1023u) {
+        if (tid == 0 && rank == 0 && mt == 0 && chunk == 0) a.status[b] = DDT_E_CUDA;
+        return;
+    }
+    const uint32_t sQ = sbase + kOffQ, sQR = sbase + kOffQR, sRing = sbase + kOffRing, sRope = sbase + kOffRope;
     const uint32_t sBar = sbase + kOffBar;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + NUM_BARS * 8 + 4);
@@ -355,7 +332,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // arrived on here (relaxed: the init fence already releases the inits);
     // the softmax threads wait on it just before their first remote store.
     if (warp == kProducerWarp) {
-        if (lane < NUM_BARS) mbar_init(bar(lane), bar_count(lane, a.kv_index != nullptr));
+        for (int i = lane; i < NUM_BARS; i += 32) mbar_init(bar(i), bar_count(i, a.kv_index != nullptr));
         if (lane == 0) *abort_flag = 0;
         mbar_fence_init();
         __syncwarp();
@@ -363,11 +340,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_kv);
             tma_prefetch_desc(&tm_kr);
+            tma_prefetch_desc(&tm_qr);
             const int qrow = b * a.Qc * a.H + mt * kRows;
-            mbar_arrive_expect_tx(bar(BAR_Q_FULL), kQSmemChunks * kChunkBytesQ);
+            mbar_arrive_expect_tx(bar(BAR_Q_FULL), kQSmemChunks * kChunkBytesQ + kQRopeBytes);
             for (int c = 0; c < kQSmemChunks; ++c)
                 tma_load_2d(sQ + c * kChunkBytesQ, &tm_q, static_cast<int>(rank) * 256 + c * 64, qrow,
                             bar(BAR_Q_FULL));
+            tma_load_2d(sQR, &tm_qr, static_cast<int>(rank) * 32, qrow, bar(BAR_Q_FULL));
         }
     } else if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -444,7 +423,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int slot = jj % kSlots, use = jj / kSlots, rs = jj % kRopeSlots;
             if (!__all_sync(0xffffffffu,
                             (use < 1 || mbar_wait(bar(BAR_RING_EMPTY + slot), (use - 1) & 1, deadline, abort_flag)) &&
-                                (jj < kRopeSlots || mbar_wait(bar(BAR_S_FULL + rs), ((jj - kRopeSlots) / kRopeSlots) & 1,
+                                (jj < kRopeSlots || mbar_wait(bar(BAR_S_FULL + (jj - kRopeSlots) % kSPBufs),
+                                                              ((jj - kRopeSlots) / kSPBufs) & 1,
                                                               deadline, abort_flag)))) {
                 ok = false;
                 break;
@@ -511,10 +491,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int jj = 0; jj < nrange; ++jj) {
                 const int slot = jj % kSlots, use = jj / kSlots, rs = jj % kRopeSlots;
-                // latent slot: PV of tile jj - 4 done; rotary slot: S of tile jj - 3 done
+                // latent slot: PV of tile jj - 4 done; rotary slot: S of tile jj - 2 done
                 if ((use >= 1 && !mbar_wait(bar(BAR_RING_EMPTY + slot), (use - 1) & 1, deadline, abort_flag)) ||
                     (jj >= kRopeSlots &&
-                     !mbar_wait(bar(BAR_S_FULL + rs), ((jj - kRopeSlots) / kRopeSlots) & 1, deadline, abort_flag))) {
+                     !mbar_wait(bar(BAR_S_FULL + (jj - kRopeSlots) % kSPBufs), ((jj - kRopeSlots) / kSPBufs) & 1,
+                                deadline, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -561,14 +542,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // commits.
         const bool leader = elect_one();
         constexpr uint32_t idS = idesc_f32acc(kRows, kKeys, 1, 0, 0);   // bf16 Q, K (K-major)
-        // operand descriptors of the query's chunk 0, of latent slot 0's
-        // chunk 0 and of rotary slot 0; the loop adds offsets / 16
-        const uint64_t dq = desc_sw128(sQ, 16, 1024), dk = desc_sw128(sRing, 16, 1024), dr = desc_sw64(sRope, 512);
+        // operand descriptors of the query's latent chunk 0 and rotary part,
+        // of latent slot 0's chunk 0 and of rotary slot 0; the loop adds
+        // offsets / 16
+        const uint64_t dq = desc_sw128(sQ, 16, 1024), dqr = desc_sw64(sQR, 512), dk = desc_sw128(sRing, 16, 1024),
+                       dr = desc_sw64(sRope, 512);
         const uint32_t dq_lo = static_cast<uint32_t>(dq), dq_hi = static_cast<uint32_t>(dq >> 32);
+        const uint32_t dqr_lo = static_cast<uint32_t>(dqr), dqr_hi = static_cast<uint32_t>(dqr >> 32);
         const uint32_t dk_lo = static_cast<uint32_t>(dk), dk_hi = static_cast<uint32_t>(dk >> 32);
         const uint32_t dr_lo = static_cast<uint32_t>(dr), dr_hi = static_cast<uint32_t>(dr >> 32);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q_FULL), 0, deadline, abort_flag) &&
-                                              mbar_wait(bar(BAR_QT_READY), 0, deadline, abort_flag));
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q_FULL), 0, deadline, abort_flag));
         tc_fence_after();
         for (int jj = 0; jj < nrange && ok; ++jj) {
             const int sb = jj % kSPBufs, slot = jj % kSlots;
@@ -584,7 +567,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (a.kv_index) fence_proxy_async_smem();
             tc_fence_after();
             const uint32_t dS = tmem + kColSP + sb * 64;
-            const uint32_t k_lo = dk_lo + ((slot * kLatBytes) >> 4), r_lo = dr_lo + ((sb * kKRopeBytes) >> 4);
+            const uint32_t k_lo = dk_lo + ((slot * kLatBytes) >> 4),
+                           r_lo = dr_lo + (((jj % kRopeSlots) * kKRopeBytes) >> 4);
             if (leader) {
 #pragma unroll
                 for (int c = 0; c < kQSmemChunks; ++c)
@@ -593,11 +577,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         mma_ss_w(dS, dq_lo + ((c * kChunkBytesQ + ks * 32) >> 4), dq_hi,
                                  k_lo + ((c * kChunkBytesKV + ks * 32) >> 4), dk_hi, idS, (c > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ts_w(dS, tmem + kColQ3 + ks * 8, k_lo + ((3 * kChunkBytesKV + ks * 32) >> 4), dk_hi, idS, 1u);
-#pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
-                    mma_ts_w(dS, tmem + kColQR + ks * 8, r_lo + ((ks * 32) >> 4), dr_hi, idS, 1u);
+                    mma_ss_w(dS, dqr_lo + ((ks * 32) >> 4), dqr_hi, r_lo + ((ks * 32) >> 4), dr_hi, idS, 1u);
                 mma_commit(bar(BAR_S_FULL + sb));
             }
             __syncwarp();
@@ -661,7 +642,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // of it (this CTA's partial scores of the row's 64 keys), block-scales
         // each key half and sends it to the partner as unit 2j + h of its
         // exchange ring, as soon as the partner has read the unit its slot
-        // held before (three units back); then it writes the scaled values
+        // held before (two units back); then it writes the scaled values
         // back in place of its own scores and releases the buffer to the
         // softmax. Dedicated warps make the transfer independent of the
         // softmax: it starts as soon as S is done and runs while the softmax
@@ -791,20 +772,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto wwait_cluster = [&](uint32_t barrier, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait_cluster(barrier, parity, deadline, abort_flag));
         };
-        // the latent query chunk 3 (warps 0-3) or rotary query (warps 4-7) of
-        // the 32 rows of lane quadrant w % 4 -> tensor memory, one row per
-        // lane, as bf16 pairs (low half = even column)
-        {
-            const uint32_t quad_base = static_cast<uint32_t>(quad * 32) << 16;
-            if (sub == 0) tmem_st32(tmem + quad_base + kColQ3, q_pre);
-            else tmem_st16(tmem + quad_base + kColQR, *reinterpret_cast<const uint32_t(*)[16]>(&q_pre[0]));
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_QT_READY));
-        }
-
-
         // the row sum of this thread's keys, as the sums of its even and odd
         // keys (one packed add per key pair)
         float m_ref = -INFINITY, l_even = 0.f, l_odd = 0.f;
@@ -1224,8 +1191,9 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
     // (with a block table the KV maps cover the pools; the gather path does
     // not use them)
     const uint64_t kv_rows = kv_index ? static_cast<uint64_t>(pool_rows) : static_cast<uint64_t>(tree.B) * in.Tcap;
-    CUtensorMap tm_q, tm_kv, tm_kr;
+    CUtensorMap tm_q, tm_qr, tm_kv, tm_kr;
     if (!encode_2d(enc, &tm_q, in.q_lat, 512, rows_total, 64, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(enc, &tm_qr, in.q_rope, 64, rows_total, 32, kRows, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !encode_2d(enc, &tm_kv, in.c_kv, 512, kv_rows, 64, kKeys, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(enc, &tm_kr, in.k_rope, 64, kv_rows, 32, kKeys, CU_TENSOR_MAP_SWIZZLE_64B))
         return DDT_E_INVAL;
@@ -1248,8 +1216,6 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
     a.mask = tree.mask;
     a.n_nodes = tree.n_nodes;
     a.prefix_len = in.prefix_len;
-    a.q_lat = static_cast<const uint16_t *>(in.q_lat);
-    a.q_rope = static_cast<const uint16_t *>(in.q_rope);
     a.status = tree.status;
     a.rows_total = rows_total;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
@@ -1276,7 +1242,7 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
                          static_cast<uint64_t>(tree.B) * plan.nsplit, kRows, a.out_bf16 != 0))
         return DDT_E_INVAL;
     dim3 grid(plan.mtiles * 2, plan.nsplit, tree.B);
-    if (launch_kernel(verify_attn_kernel, grid, dim3(kThreads), kSmemBytes, s, after_prev, tm_q, tm_kv, tm_kr, tm_o,
+    if (launch_kernel(verify_attn_kernel, grid, dim3(kThreads), kSmemBytes, s, after_prev, tm_q, tm_qr, tm_kv, tm_kr, tm_o,
                       a) != cudaSuccess)
         return DDT_E_CUDA;
     if (plan.nsplit > 1) {
