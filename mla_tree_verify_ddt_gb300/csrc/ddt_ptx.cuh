@@ -72,14 +72,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
 
 // Wait on a barrier that threads of another CTA of the cluster arrive on
 // (their arrivals release at cluster scope, so this acquires at cluster scope).
+// No suspend-time hint here: these are the exchange's waits, on the chain
+// that sets the attention's tile period, and a suspended thread resumed late
+// enough to cost 3-6% of the call.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "n"(kWaitSuspendNs)
+        : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
 }
