@@ -536,8 +536,8 @@ def side_legs(bn: Bench, w: Workload, n, attn_ms, wl_idx):
     paged_ms = bn.mean_ms(gp, n)
     legs["paged_attn"] = {"us": paged_ms * 1e3, "tflops": flop / (paged_ms / 1e3) / 1e12,
                           "vs_contiguous": attn_ms / paged_ms, "pool_rows": n_pool,
-                          "note": "block table of page size 1 over a shuffled pool; the producer warp "
-                                  "gathers rows with cp.async"}
+                          "note": "block table of page size 1 over a shuffled pool; two warps gather the rows "
+                                  "with cp.async, reading the block table two tiles ahead"}
     del pool_kv, pool_kr, kv_index, perm, gp
 
     # ---- the KV commit after accept (the append of the accepted path's keys),

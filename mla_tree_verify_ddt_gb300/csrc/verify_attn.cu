@@ -293,6 +293,10 @@ __device__ __forceinline__ void dequantize_pair(uint32_t w, float d, float &v0, 
     mul_f32x2(q0, q1, d, d, v0, v1);
 }
 
+// kPaged: the instantiation launched for a block-table cache (a.kv_index set),
+// whose gather warps read the block table two tiles ahead; the contiguous
+// instantiation runs the tensor-map loads.
+template <bool kPaged>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
                        const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kr,
@@ -419,6 +423,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int kend_g = (t_ok && static_cast<long long>(T) + n_g <= a.Tcap) ? T + n_g : 0;
         const int32_t *kvi = a.kv_index + static_cast<size_t>(b) * a.Tcap;
         bool ok = true, bad_index = false;
+        // Block-table entries are loaded two tiles ahead and checked only
+        // when their tile is copied, so a load's latency overlaps the slot
+        // waits instead of sitting between a slot's release and its copies.
+        auto entry = [&](int jj) {
+            const int key = (t0 + jj) * kKeys + k_lo + lane;
+            return (jj < nrange && key < a.Tcap) ? kvi[key] : 0;
+        };
+        int e_next = 0, e_next2 = 0;
+        if constexpr (kPaged) {
+            e_next = entry(0);
+            e_next2 = entry(1);
+        }
         for (int jj = 0; jj < nrange; ++jj) {
             const int slot = jj % kSlots, use = jj / kSlots, rs = jj % kRopeSlots;
             if (!__all_sync(0xffffffffu,
@@ -432,7 +448,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t dst = sRing + slot * kLatBytes, rdst = sRope + rs * kKRopeBytes;
             // pool row of key k_lo + lane of the tile
             const int key = (t0 + jj) * kKeys + k_lo + lane;
-            int phys = key < a.Tcap ? kvi[key] : 0;
+            int phys;
+            if constexpr (kPaged) {
+                phys = e_next;
+                e_next = e_next2;
+                e_next2 = entry(jj + 2);
+            } else {
+                phys = key < a.Tcap ? kvi[key] : 0;
+            }
             if (phys < 0 || phys >= a.pool_rows) {
                 if (key < kend_g) bad_index = true;
                 phys = 0;
@@ -1201,8 +1224,11 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(verify_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(verify_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kSmemBytes);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(verify_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            kSmemBytes);
     });
     if (attr_err != cudaSuccess) return DDT_E_CUDA;
 
@@ -1242,8 +1268,8 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
                          static_cast<uint64_t>(tree.B) * plan.nsplit, kRows, a.out_bf16 != 0))
         return DDT_E_INVAL;
     dim3 grid(plan.mtiles * 2, plan.nsplit, tree.B);
-    if (launch_kernel(verify_attn_kernel, grid, dim3(kThreads), kSmemBytes, s, after_prev, tm_q, tm_qr, tm_kv, tm_kr, tm_o,
-                      a) != cudaSuccess)
+    if (launch_kernel(kv_index ? verify_attn_kernel<true> : verify_attn_kernel<false>, grid, dim3(kThreads), kSmemBytes,
+                      s, after_prev, tm_q, tm_qr, tm_kv, tm_kr, tm_o, a) != cudaSuccess)
         return DDT_E_CUDA;
     if (plan.nsplit > 1) {
         auto merge = plan.nsplit <= 4 ? merge_chunks_kernel<4>
