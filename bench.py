@@ -75,11 +75,19 @@ def load_peaks():
     return FALLBACK_PEAKS["hbm_gbs"], FALLBACK_PEAKS["bf16_tflops"], "fallback"
 
 
+HOST_SIDE_MARK = b"// ---------------------------------------------------------------- host side"
+
+
 def kernel_source_hash() -> str:
+    """Hash of the attention kernel's device source: verify_attn.cu up to its
+    host-side section, and the PTX helpers it includes."""
     h = hashlib.sha256()
     for f in ("verify_attn.cu", "ddt_ptx.cuh"):
         with open(os.path.join(ROOT, "mla_tree_verify_ddt_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+            data = fh.read()
+        if HOST_SIDE_MARK in data:
+            data = data[:data.index(HOST_SIDE_MARK)]
+        h.update(data)
     return h.hexdigest()[:16]
 
 

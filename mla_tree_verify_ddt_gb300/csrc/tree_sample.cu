@@ -753,22 +753,33 @@ const SampleKernel kKernels[2][6] = {
 static_assert(kSampleMaxRows == 11, "one kernel per odd R up to kSampleMaxRows");
 }  // namespace
 
+// The largest cluster the sampling kernels may use on the current device (0
+// if their attributes could not be set: tried again on the next call), found
+// once per device.
 int sample_max_cluster() {
-    static std::once_flag once;
-    static int max_c = 0;
-    std::call_once(once, [] {
-        const int smem_max = static_cast<int>(smem_bytes(kSampleMaxRows, kSampleMaxRegions));
-        for (auto &row : kKernels)
-            for (SampleKernel k : row)
-                if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess)
-                    return;
-        max_c = 8;
-        for (auto &row : kKernels)
-            for (SampleKernel k : row)
-                if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-                    cudaGetLastError();
-                    return;
-                }
+    constexpr int kDevices = 64;
+    static std::mutex mu;
+    static int known[kDevices];  // 0: not yet found
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (known[dev] > 0) return known[dev];
+    const int smem_max = static_cast<int>(smem_bytes(kSampleMaxRows, kSampleMaxRegions));
+    for (auto &row : kKernels)
+        for (SampleKernel k : row)
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess) {
+                cudaGetLastError();
+                return 0;
+            }
+    int max_c = 8;
+    bool nonportable = true;
+    for (auto &row : kKernels)
+        for (SampleKernel k : row)
+            if (nonportable && cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+                cudaGetLastError();
+                nonportable = false;
+            }
+    if (nonportable) {
         // a cluster of 16 CTAs of the size the 16-CTA plans use
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(16);
@@ -785,7 +796,8 @@ int sample_max_cluster() {
         if (cudaOccupancyMaxActiveClusters(&n, kKernels[0][kSampleMaxRows / 2], &cfg) == cudaSuccess && n > 0)
             max_c = 16;
         cudaGetLastError();
-    });
+    }
+    known[dev] = max_c;
     return max_c;
 }
 

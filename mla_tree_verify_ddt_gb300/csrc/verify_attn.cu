@@ -1143,6 +1143,24 @@ EncodeTiledFn get_encoder() {
     return fn;
 }
 
+// The kernels' dynamic shared-memory size, set once per device (and tried
+// again on the next call if setting it failed).
+cudaError_t set_attn_attributes() {
+    constexpr int kDevices = 64;
+    static std::mutex mu;
+    static bool done[kDevices];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(verify_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(verify_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
+}
+
 // bf16 matrix [rows, cols] row-major, box [box_rows, box_cols]
 bool encode_2d(EncodeTiledFn enc, CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows,
                uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
@@ -1221,16 +1239,7 @@ int launch_verify_attn(const ddt_attn_in &in, const ddt_tree &tree, float scale,
         !encode_2d(enc, &tm_kr, in.k_rope, 64, kv_rows, 32, kKeys, CU_TENSOR_MAP_SWIZZLE_64B))
         return DDT_E_INVAL;
 
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(verify_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kSmemBytes);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(verify_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return DDT_E_CUDA;
+    if (set_attn_attributes() != cudaSuccess) return DDT_E_CUDA;
 
     AttnArgs a{};
     a.B = tree.B;
