@@ -587,7 +587,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             // gathered tiles were written by ordinary (generic-proxy)
             // copies: order them before the tensor core's reads
-            if (a.kv_index) fence_proxy_async_smem();
+            if constexpr (kPaged) fence_proxy_async_smem();
             tc_fence_after();
             const uint32_t dS = tmem + kColSP + sb * 64;
             const uint32_t k_lo = dk_lo + ((slot * kLatBytes) >> 4),
